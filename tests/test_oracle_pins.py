@@ -1,0 +1,262 @@
+"""Pins of the fp64 oracle to facts other than itself (CPU only).
+
+Each test checks the oracle against a closed form, an invariant, a brute-force
+construction, or values worked by hand, chosen so that a plausible slip in the
+oracle -- a dropped term, a wrong sign or index, a transposed state, a decay
+applied at the wrong token -- fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rel(x, ref):
+    return float(np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-300))
+
+
+def _rand_case(rng, lengths, H, dk, dv, unit_k=True, h0=True, gate_scale=0.1):
+    T = sum(lengths)
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    if unit_k:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+        q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    la = -np.log1p(np.exp(rng.standard_normal((T, H)))) * gate_scale
+    b = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    s0 = rng.standard_normal((len(lengths), H, dk, dv)) * 0.3 if h0 else None
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    return q, k, v, la, b, s0, cu
+
+
+# --- hand-worked values -----------------------------------------------------
+
+def test_hand_cases():
+    with open(os.path.join(GOLD, "hand_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        o, hT = oracle.gdn(np.array(c["q"]), np.array(c["k"]), np.array(c["v"]),
+                           np.array(c["log_alpha"]), np.array(c["beta"]),
+                           np.array(c["h0"]), np.array(c["cu_seqlens"]))
+        np.testing.assert_allclose(o, np.array(c["o"]), rtol=0, atol=1e-14, err_msg=c["name"])
+        np.testing.assert_allclose(hT, np.array(c["hT"]), rtol=0, atol=1e-14, err_msg=c["name"])
+        # the chunked evaluation agrees on the same hand cases (chunk 1 and 64)
+        for C in (1, 64):
+            oc, hc = oracle.chunked(np.array(c["q"]), np.array(c["k"]), np.array(c["v"]),
+                                    np.array(c["log_alpha"]), np.array(c["beta"]),
+                                    np.array(c["h0"]), np.array(c["cu_seqlens"]), chunk=C)
+            np.testing.assert_allclose(oc, np.array(c["o"]), rtol=0, atol=1e-14)
+            np.testing.assert_allclose(hc, np.array(c["hT"]), rtol=0, atol=1e-14)
+
+
+# --- P1: linear attention equals its quadratic masked form -------------------
+
+@pytest.mark.parametrize("lengths,dk,dv", [([7], 3, 5), ([1, 9, 4], 4, 4), ([33, 0, 17], 8, 6)])
+def test_linear_matches_quadratic_form(lengths, dk, dv):
+    rng = np.random.default_rng(1)
+    q, k, v, _, _, s0, cu = _rand_case(rng, lengths, 2, dk, dv, unit_k=False)
+    o, hT = oracle.linear(q, k, v, s0, cu)
+    oq, hq = oracle.linear_quadratic(q, k, v, s0, cu)
+    assert _rel(o, oq) < 1e-13
+    assert _rel(hT, hq) < 1e-13
+
+
+def test_linear_quadratic_is_brute_force_sum():
+    # (Q K^T ⊙ M) V written as the explicit double sum, tiny case
+    rng = np.random.default_rng(2)
+    T, dk, dv = 5, 2, 3
+    q = rng.standard_normal((T, 1, dk)); k = rng.standard_normal((T, 1, dk))
+    v = rng.standard_normal((T, 1, dv))
+    oq, _ = oracle.linear_quadratic(q, k, v)
+    for t in range(T):
+        ref = sum(float(q[t, 0] @ k[s, 0]) * v[s, 0] for s in range(t + 1))
+        np.testing.assert_allclose(oq[t, 0], ref, rtol=1e-14, atol=1e-14)
+
+
+# --- P2: with ||k||=1 and beta=1 the updated state stores v under key k ------
+
+@pytest.mark.parametrize("dk,dv", [(3, 5), (16, 16), (64, 8)])
+def test_delta_rule_overwrite_invariant(dk, dv):
+    rng = np.random.default_rng(3)
+    q, k, v, la, _, s0, cu = _rand_case(rng, [11, 6], 3, dk, dv, gate_scale=1.0)
+    beta = np.ones(la.shape)
+    # o_t = S_t q_t, so asking with q_t = k_t reads back S_t k_t, which must be v_t
+    o, _ = oracle.gdn(k, k, v, la, beta, s0, cu)
+    assert np.max(np.abs(o - v)) < 1e-13
+    # and through the chunked form
+    oc, _ = oracle.chunked(k, k, v, la, beta, s0, cu, chunk=4)
+    assert np.max(np.abs(oc - v)) < 1e-12
+    # with beta < 1 the invariant must NOT hold (the test has teeth)
+    o2, _ = oracle.gdn(k, k, v, la, beta * 0.5, s0, cu)
+    assert np.max(np.abs(o2 - v)) > 1e-3
+
+
+# --- P3: chunk-wise evaluation equals the token recurrence -------------------
+
+@pytest.mark.parametrize("C", [1, 4, 16, 64])
+@pytest.mark.parametrize("delta", [True, False])
+def test_chunked_equals_recurrent(C, delta):
+    rng = np.random.default_rng(4)
+    lengths = [1, 70, 0, 129, 64, 5]
+    q, k, v, la, b, s0, cu = _rand_case(rng, lengths, 2, 8, 6)
+    o, hT = oracle.recurrent(q, k, v, la, b, s0, cu, delta_rule=delta)
+    oc, hc = oracle.chunked(q, k, v, la, b, s0, cu, chunk=C, delta_rule=delta)
+    assert _rel(oc, o) < 1e-12
+    assert _rel(hc, hT) < 1e-12
+
+
+def test_chunked_strong_gates():
+    # strongly negative log-gates: the chunked form must not form exp(g_i)*exp(-g_j)
+    rng = np.random.default_rng(5)
+    q, k, v, la, b, s0, cu = _rand_case(rng, [150], 1, 8, 8)
+    la = la * 0 - 30.0  # alpha = e^-30 per token: g reaches -1920 in a 64-chunk
+    o, hT = oracle.gdn(q, k, v, la, b, s0, cu)
+    oc, hc = oracle.chunked(q, k, v, la, b, s0, cu, chunk=64)
+    assert np.all(np.isfinite(oc))
+    assert _rel(oc, o) < 1e-12 and _rel(hc, hT) < 1e-12
+
+
+# --- P4: beta = 0 leaves only the decayed initial state ----------------------
+
+def test_beta_zero_closed_form():
+    rng = np.random.default_rng(6)
+    q, k, v, la, _, s0, cu = _rand_case(rng, [9, 4], 2, 5, 3)
+    beta = np.zeros(la.shape)
+    o, hT = oracle.gdn(q, k, v, la, beta, s0, cu)
+    for s in range(2):
+        a, e = cu[s], cu[s + 1]
+        for h in range(2):
+            G = np.cumsum(la[a:e, h])
+            ref = np.exp(G)[:, None] * (q[a:e, h] @ s0[s, h])
+            np.testing.assert_allclose(o[a:e, h], ref, rtol=1e-13, atol=1e-15)
+            np.testing.assert_allclose(hT[s, h], np.exp(G[-1]) * s0[s, h], rtol=1e-13)
+
+
+# --- P5: decay without the delta term has a masked closed form ---------------
+
+def test_decay_without_delta_closed_form():
+    rng = np.random.default_rng(7)
+    q, k, v, la, b, s0, cu = _rand_case(rng, [12], 1, 4, 3, unit_k=False, gate_scale=0.5)
+    o, hT = oracle.recurrent(q, k, v, la, b, s0, cu, delta_rule=False)
+    G = np.cumsum(la[:, 0])
+    D = np.tril(np.exp(G[:, None] - G[None, :]))
+    Q, K, V = q[:, 0], k[:, 0], v[:, 0] * b[:, 0:1]
+    ref = (Q @ K.T * D) @ V + np.exp(G)[:, None] * (Q @ s0[0, 0])
+    np.testing.assert_allclose(o[:, 0], ref, rtol=1e-12, atol=1e-13)
+    refh = np.exp(G[-1]) * s0[0, 0] + (K * np.exp(G[-1] - G)[:, None]).T @ V
+    np.testing.assert_allclose(hT[0, 0], refh, rtol=1e-12, atol=1e-13)
+
+
+# --- P7: explicit solution of the linear recurrence on tiny inputs -----------
+
+def test_transition_matrix_product():
+    rng = np.random.default_rng(8)
+    T, dk, dv = 6, 3, 2
+    q, k, v, la, b, s0, cu = _rand_case(rng, [T], 1, dk, dv, unit_k=False, gate_scale=1.0)
+    o, hT = oracle.gdn(q, k, v, la, b, s0, cu)
+    # S_t = S_{t-1} M_t + b_t v_t k_t^T with M_t = a_t (I - b_t k_t k_t^T) (dk x dk)
+    M = [math.exp(la[t, 0]) * (np.eye(dk) - b[t, 0] * np.outer(k[t, 0], k[t, 0])) for t in range(T)]
+    S0 = s0[0, 0].T
+    for t in range(T):
+        # S_t = S0 M_1..M_t + sum_{r<=t} b_r v_r k_r^T M_{r+1}..M_t
+        P = np.eye(dk)
+        for r in range(t + 1):
+            P = P @ M[r]
+        St = S0 @ P
+        for r in range(t + 1):
+            Pr = np.eye(dk)
+            for x in range(r + 1, t + 1):
+                Pr = Pr @ M[x]
+            St = St + b[r, 0] * np.outer(v[r, 0], k[r, 0]) @ Pr
+        np.testing.assert_allclose(o[t, 0], St @ q[t, 0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(hT[0, 0], St.T, rtol=1e-12, atol=1e-13)
+
+
+# --- P8: sequences are independent; h_T chains into h0 ----------------------
+
+def test_varlen_packing_and_state_chaining():
+    rng = np.random.default_rng(9)
+    lengths = [5, 0, 13, 2]
+    q, k, v, la, b, s0, cu = _rand_case(rng, lengths, 2, 4, 4)
+    o, hT = oracle.gdn(q, k, v, la, b, s0, cu)
+    for s in range(len(lengths)):
+        a, e = cu[s], cu[s + 1]
+        os_, hs = oracle.gdn(q[a:e], k[a:e], v[a:e], la[a:e], b[a:e], s0[s:s + 1])
+        np.testing.assert_array_equal(o[a:e], os_)
+        np.testing.assert_array_equal(hT[s:s + 1], hs)
+    # a zero-length sequence returns its initial state
+    np.testing.assert_array_equal(hT[1], s0[1])
+    # splitting sequence 2 in two calls, h_T of the first as h0 of the second
+    a, e = cu[2], cu[3]
+    m = a + 6
+    o1, h1 = oracle.gdn(q[a:m], k[a:m], v[a:m], la[a:m], b[a:m], s0[2:3])
+    o2, h2 = oracle.gdn(q[m:e], k[m:e], v[m:e], la[m:e], b[m:e], h1)
+    np.testing.assert_allclose(np.concatenate([o1, o2]), o[a:e], rtol=0, atol=0)
+    np.testing.assert_allclose(h2, hT[2:3], rtol=0, atol=0)
+
+
+# --- P9: the per-chunk affine maps compose to the final state ----------------
+
+def test_affine_chunk_maps_compose():
+    """SparseGDN article, "Схема встраивания селектора…": each chunk acts on the
+    state as an affine map S -> A_c S + B_c.  In h = S^T form, from the chunked
+    oracle's w, u, g:  h -> (e^{g_C} I - K~^T W) h + K~^T U  with K~ = e^{g_C-g} K."""
+    rng = np.random.default_rng(10)
+    C = 8
+    lengths = [29]
+    q, k, v, la, b, s0, cu = _rand_case(rng, lengths, 1, 6, 5)
+    _, hT = oracle.gdn(q, k, v, la, b, s0, cu)
+    _, _, it = oracle.chunked(q, k, v, la, b, s0, cu, chunk=C, intermediates=True)
+    h = s0[0, 0].copy()
+    for c0 in range(0, lengths[0], C):
+        c1 = min(c0 + C, lengths[0])
+        g = it["g"][c0:c1, 0]
+        Kt = k[c0:c1, 0] * np.exp(g[-1] - g)[:, None]
+        Mc = np.exp(g[-1]) * np.eye(6) - Kt.T @ it["w"][c0:c1, 0]
+        Bc = Kt.T @ it["u"][c0:c1, 0]
+        h = Mc @ h + Bc
+    assert _rel(h, hT[0, 0]) < 1e-12
+
+
+def test_wy_intermediates_solve_the_delta_system():
+    # Tm really is (I + A)^-1 and A is the beta-scaled, decay-masked K K^T
+    rng = np.random.default_rng(11)
+    q, k, v, la, b, s0, cu = _rand_case(rng, [40], 1, 8, 4)
+    _, _, it = oracle.chunked(q, k, v, la, b, s0, cu, chunk=16, intermediates=True)
+    for c in range(3):
+        A, Tm = it["A"][c, 0], it["Tm"][c, 0]
+        n = min(16, 40 - 16 * c)
+        np.testing.assert_allclose(Tm @ (np.eye(16) + A), np.eye(16), atol=1e-12)
+        t0 = 16 * c
+        for i in range(n):
+            for j in range(16):
+                expect = 0.0
+                if j < i:
+                    gi = np.sum(la[t0:t0 + i + 1, 0]); gj = np.sum(la[t0:t0 + j + 1, 0])
+                    expect = b[t0 + i, 0] * np.exp(gi - gj) * (k[t0 + i, 0] @ k[t0 + j, 0])
+                assert abs(A[i, j] - expect) < 1e-13
+
+
+def test_decode_step_equals_one_prefill_token():
+    rng = np.random.default_rng(12)
+    B, H, dk, dv = 3, 2, 5, 4
+    q, k, v, la, b, s0, cu = _rand_case(rng, [1] * B, H, dk, dv)
+    o, st = oracle.decode_step(q, k, v, la, b, s0)
+    for i in range(B):
+        o1, h1 = oracle.gdn(q[i:i + 1], k[i:i + 1], v[i:i + 1], la[i:i + 1], b[i:i + 1], s0[i:i + 1])
+        np.testing.assert_array_equal(o[i:i + 1], o1)
+        np.testing.assert_array_equal(st[i:i + 1], h1)
+
+
+def test_oracle_rejects_bad_seqlens():
+    rng = np.random.default_rng(13)
+    q, k, v, la, b, s0, cu = _rand_case(rng, [4, 4], 1, 2, 2)
+    with pytest.raises(ValueError):
+        oracle.gdn(q, k, v, la, b, s0, np.array([0, 5, 3, 8]))
