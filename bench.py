@@ -1,0 +1,337 @@
+"""Benchmark: GDN long prefill on B300, tokens/s and fraction of roofline.
+
+Workload: 4 packed sequences with seeded lengths summing to T = 131072 tokens,
+H = 32 heads, dk = dv = 128, bf16 q/k/v/o, fp32 gates and states, chunk 64
+(one gdn_chunk_fwd call per step).  Inputs are seeded synthetic tensors far
+larger than L2 (4.35 GB), so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line is printed by rank 0.  Under torchrun each rank runs the same
+per-GPU workload on its own GPU (weak scaling, no collective on the data
+path); `value` is the total tokens of all ranks over the slowest rank's time.
+`--impl reference` times the fp64 CPU oracle instead, on a bounded sample.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdn_inputs as gi  # noqa: E402
+
+METRIC = "GDN prefill tokens/s at H=32,d=128,T=128K bf16; % of roofline (1×B300)"
+T_TOTAL, H, D = 131072, 32, 128
+LENGTHS = gi.varlen_lengths(T_TOTAL, 4, 0)
+WORKLOAD = "gdn_varlen_t131072_h32_d128"
+
+
+def alg_bytes():
+    """Algorithmic bytes of one call: q, k, v in and o out (bf16), the two fp32
+    gates, h0 in and h_T out (fp32)."""
+    n = len(LENGTHS)
+    return (4 * T_TOTAL * H * D * 2) + (2 * T_TOTAL * H * 4) + (2 * n * H * D * D * 4)
+
+
+def alg_flops():
+    """Algorithmic flops per token per head at chunk 64, d = 128: three state
+    contractions (w h, q h, k~^T v_new: 6 d^2), the causal halves of the five
+    chunk-local products (5 C d) and the triangular solve (C^2 / 3)."""
+    C = 64
+    return T_TOTAL * H * (6 * D * D + 5 * C * D + C * C / 3)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]), src="measured")
+    return dict(hbm=6400.0, bf16=1800.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(budget_s=15.0):
+    """The fp64 oracle (as it stands) on a bounded sample of the workload: the
+    first S tokens of each of the 4 sequences, all 32 heads; S is grown until
+    one run takes a few seconds, then the rate is measured on one larger run."""
+    import oracle
+    inp = gi.gdn_inputs(LENGTHS, H, D, D, "bf16", h0_std=0.01, seed=0)
+    cu = inp["cu_seqlens"].tolist()
+
+    def sample(S):
+        idx = []
+        lens = []
+        for s in range(len(LENGTHS)):
+            n = min(S, LENGTHS[s])
+            idx.extend(range(cu[s], cu[s] + n))
+            lens.append(n)
+        sl = lambda x: x[idx].contiguous()
+        cus = [0]
+        for n in lens:
+            cus.append(cus[-1] + n)
+        return (sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["log_alpha"]), sl(inp["beta"]),
+                inp["h0"], cus), sum(lens)
+
+    S, elapsed, tokens = 16, 0.0, 0
+    while True:
+        args, tokens = sample(S)
+        t0 = time.perf_counter()
+        oracle.gdn(*args)
+        elapsed = time.perf_counter() - t0
+        if elapsed > budget_s / 4 or S >= max(LENGTHS):
+            break
+        S = min(max(LENGTHS), int(S * max(2.0, (budget_s / 2) / max(elapsed, 1e-3))))
+    return {"value": tokens / elapsed, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "host_cpus": os.cpu_count(), "kind": "oracle", "seconds": elapsed,
+            "sample": "fp64 token recurrence on the first %d tokens of each of the 4 sequences, "
+                      "all 32 heads (%d tokens x 32 heads)" % (S, tokens)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    inp = gi.gdn_inputs(LENGTHS, H, D, D, "bf16", h0_std=0.01, seed=0)
+    cu = inp["cu_seqlens"].tolist()
+    S = 256  # tokens of each sequence per step: a bounded sample of the workload
+    idx = [t for s in range(4) for t in range(cu[s], cu[s] + S)]
+    sl = lambda x: x[idx].contiguous()
+    step_args = (sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["log_alpha"]), sl(inp["beta"]),
+                 inp["h0"], [0, S, 2 * S, 3 * S, 4 * S])
+    for _ in range(args.warmup):
+        oracle.gdn(*step_args)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gdn(*step_args)
+    dt = (time.perf_counter() - t0) / args.steps
+    tokens = 4 * S
+    value = tokens / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_TOTAL, "H": H, "dk": D, "dv": D,
+                   "seq_lens": LENGTHS, "chunk": 64},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": "first %d tokens of each of the 4 sequences, all 32 heads, "
+                                   "per step" % S},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import gated_deltanet_sequence_prefill_b300 as g
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    inp = gi.gdn_inputs(LENGTHS, H, D, D, "bf16", h0_std=0.01, seed=0)
+    dv = {k: v.cuda() for k, v in inp.items()}
+    T = T_TOTAL
+    n = len(LENGTHS)
+    o = torch.empty(T, H, D, dtype=torch.bfloat16, device="cuda")
+    hT = torch.empty(n, H, D, D, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(g.chunk_fwd_workspace_size(T, H, D, D, n), 256), dtype=torch.uint8,
+                     device="cuda")
+    fused = g.chunk_fwd_workspace_size(T, H, D, D, n) < g.staged_workspace_size(T, H, D, D, n)
+    launches_per_call = 2 if fused else 4
+    stream = torch.cuda.current_stream()
+
+    def call():
+        g.gdn_chunk_fwd(dv["q"], dv["k"], dv["v"], dv["log_alpha"], dv["beta"], dv["h0"],
+                        dv["cu_seqlens"], o=o, h_T=hT, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    assert g.workspace_status(ws) == 0
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    per_call = [a.elapsed_time(b) for a, b in ev]
+    status = g.workspace_status(ws)
+    if status != 0:
+        raise RuntimeError("device status %d" % status)
+
+    ms = torch.tensor([total_ms / args.steps], device="cuda")
+    if dist is not None:
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    ms_per_step = float(ms.item())
+    value = world * T / (ms_per_step / 1e3)
+
+    # end to end through the same public call, from and to pinned host memory
+    host = {k: v.pin_memory() for k, v in inp.items()}
+    o_host = torch.empty(T, H, D, dtype=torch.bfloat16).pin_memory()
+    h_host = torch.empty(n, H, D, D, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = o_host.numel() * 2 + h_host.numel() * 4
+    e2e_steps = max(1, min(args.steps, 5))
+
+    def e2e_call():
+        dd = {k: v.to("cuda", non_blocking=True) for k, v in host.items()}
+        oo, hh, _ = g.gdn_chunk_fwd(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["beta"], dd["h0"],
+                                    dd["cu_seqlens"], workspace=ws)
+        o_host.copy_(oo, non_blocking=True)
+        h_host.copy_(hh, non_blocking=True)
+
+    e2e_call()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_call()
+    e1.record(stream)
+    barrier()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1) / e2e_steps], device="cuda")
+    if dist is not None:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = world * T / (float(e2e_ms.item()) / 1e3)
+
+    if rank == 0:
+        pk = peaks()
+        kern_ms = statistics.median(per_call)
+        achieved = alg_bytes() / (kern_ms / 1e3) / 1e9
+        traffic = None
+        prof = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(prof):
+            with open(prof) as f:
+                t = json.load(f)
+            if t.get("kernel_set") == ("fused" if fused else "staged"):
+                traffic = t.get("bytes_per_call")
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
+                    "log_alpha=-softplus(N)*0.1, beta=sigmoid(N), h0 N(0,0.01))",
+            "config": {"workload": WORKLOAD, "T": T, "H": H, "dk": D, "dv": D, "seq_lens": LENGTHS,
+                       "chunk": 64, "path": "fused" if fused else "staged",
+                       "l2": "inputs larger than L2 (%.2f GB per call), no flush" % (alg_bytes() / 1e9)},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm"], "traffic": traffic,
+                         "peak_source": pk["src"],
+                         "kernel_ms": kern_ms,
+                         "roofline_ms": 1e3 * max(alg_bytes() / (pk["hbm"] * 1e9),
+                                                  alg_flops() / (pk["bf16"] * 1e12)),
+                         "note": "algorithmic bytes / median duration of one gdn_chunk_fwd call "
+                                 "(plan kernel + prefill kernels), CUDA events on its stream"},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": launches_per_call * args.steps,
+            "clocks": clk.summary(),
+        }
+        line["roofline"]["frac_of_time_roofline"] = line["roofline"]["roofline_ms"] / kern_ms
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,9 @@
+"""B300 (sm_103a) gated delta rule and causal linear attention prefill.
+
+The computation runs in hand-written CUDA kernels in libgdn_b300.so behind the
+C ABI of include/gdn.h; this package is its thin PyTorch-tensor binding.
+"""
+from ._lib import (CHUNK, GdnError, chunk_fwd_workspace_size, gdn_chunk_fwd,  # noqa: F401
+                   gdn_chunk_fwd_staged, gdn_chunk_prepare, gdn_recurrent_step, lib,
+                   linear_attn_fwd, staged_workspace_size, status_string, version,
+                   workspace_status, LIB_PATH)

@@ -1,0 +1,54 @@
+// launch.h -- host-side launchers of the kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Arguments common to the prefill paths (device pointers; see gdn.h).
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const float* beta;
+    const float* h0;
+    const int32_t* cu_seqlens;
+    int n_seqs;
+    int64_t T_total;
+    int H, dk, dv;
+    gdn_dtype io;
+    bool delta_rule;  // false: plain linear attention (no gates, no delta term)
+    void* o;
+    float* h_T;
+    char* ws;
+};
+
+// Intermediates of the staged path (fp32, all in the workspace unless the
+// caller supplies its own buffers).
+struct StagedBuffers {
+    float* g;  // [T][H]
+    float* A;  // [max_chunks][H][64][64]
+    float* w;  // [T][H][dk]
+    float* u;  // [T][H][dv]
+};
+
+size_t staged_intermediate_bytes(int64_t T, int H, int dk, int dv, int n_seqs);
+StagedBuffers staged_buffers(char* ws, int64_t T, int H, int dk, int dv, int n_seqs);
+
+cudaError_t launch_plan(const int32_t* cu, int n_seqs, int64_t T_total, void* ws, cudaStream_t st);
+cudaError_t launch_kkt(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
+cudaError_t launch_wy(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
+cudaError_t launch_state_ffma(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
+cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* log_alpha,
+                          const void* beta, float* state, void* o, int B, int H, int dk, int dv,
+                          cudaStream_t st);
+
+// Fused single-kernel prefill (bf16, dk = dv = 128): tcgen05 + TMA.
+bool fused_supported(const PrefillArgs& a);
+cudaError_t launch_fused(const PrefillArgs& a, cudaStream_t st);
+
+}  // namespace gdn

@@ -1,0 +1,175 @@
+/*
+ * gdn.h -- C ABI of the B300 (sm_103a) gated-delta-rule / linear-attention
+ * library libgdn_b300.so.
+ *
+ * The operation (the gated delta rule, "GDN"), per sequence and head:
+ *     S_t = a_t * S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   o_t = S_t q_t
+ * with a_t = exp(log_alpha_t) and b_t = beta_t.  GatedDeltaNet is named among
+ * the gated linear-attention variants in the forpes.ru survey of linear
+ * attention (section "Введение"; its update table was lost in extraction);
+ * the plain rule S_t = S_{t-1} + v_t k_t^T is printed in "Как ускорить LLM на
+ * длинном контексте" (section "Linear attention").  Prefill is evaluated chunk
+ * by chunk as the SparseGDN article describes ("Чем дорог префилл в Gated
+ * Delta Networks…"): an intra-chunk delta-system solve, a sequential per-head
+ * pass over chunks, and each chunk's outputs from the state at its start.
+ *
+ * Conventions shared by every entry point
+ *  - Device pointers unless stated otherwise.  The caller owns every buffer;
+ *    the library never allocates device memory (it only sets kernel
+ *    attributes once per process).
+ *  - Token-major packed layout: q, k [T_total][H][dk], v, o [T_total][H][dv],
+ *    log_alpha, beta [T_total][H].  Sequences are delimited by cu_seqlens
+ *    (int32, device, n_seqs + 1 entries, cu[0] = 0, non-decreasing,
+ *    cu[n_seqs] = T_total).  cu_seqlens == NULL means one sequence of
+ *    T_total tokens (n_seqs must then be 1).  Zero-length sequences are
+ *    allowed: their final state is their initial state.
+ *  - The state is stored transposed, h = S^T, as fp32 [n_seqs][H][dk][dv]
+ *    row-major.  h0 == NULL means a zero initial state; h_T == NULL skips
+ *    the final-state write.
+ *  - o_t uses the state after token t's update.  q is not scaled by
+ *    1/sqrt(dk): callers pre-scale it if they want that.
+ *  - Supported head sizes: dk, dv in {64, 128}; anything else returns
+ *    GDN_ERR_UNSUPPORTED.  There is no CPU fallback.
+ *  - All calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  The returned status reports argument errors
+ *    (checked on the host, nothing is launched then) and launch errors.
+ *    Errors found on the device (a malformed cu_seqlens, a device wait that
+ *    ran out) are written to a status word in the workspace, read with
+ *    gdn_workspace_status() after the stream's work completes; when it is
+ *    non-zero the outputs of that call are unspecified.
+ *  - Alignment: q, k, v, o, h0, h_T, state must be 16-byte aligned;
+ *    log_alpha, beta 4-byte; the workspace 256-byte.
+ *  - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef GDN_B300_H
+#define GDN_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_NULL = -1,        /* a required pointer is NULL */
+    GDN_ERR_ALIGN = -2,       /* a pointer is not aligned as required */
+    GDN_ERR_SHAPE = -3,       /* negative or inconsistent sizes */
+    GDN_ERR_SEQLENS = -4,     /* cu_seqlens malformed (device-detected) */
+    GDN_ERR_DTYPE = -5,       /* unknown io dtype */
+    GDN_ERR_UNSUPPORTED = -6, /* head size or dtype combination not built */
+    GDN_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than the query */
+    GDN_ERR_CUDA = -8,        /* a CUDA runtime call or launch failed */
+    GDN_ERR_TIMEOUT = -9      /* a bounded device-side wait ran out */
+} gdn_status;
+
+typedef enum { GDN_BF16 = 0, GDN_FP32 = 1 } gdn_dtype;
+
+/* Message for a status code (static string, never NULL). */
+GDN_API const char *gdn_status_string(int status);
+
+/* Library build identifier: "<version> sm_103a". */
+GDN_API const char *gdn_version(void);
+
+/*
+ * Workspace bytes needed by gdn_chunk_fwd for these sizes (0 on bad sizes).
+ * The bf16 path with dk = dv = 128 keeps every intermediate on-chip and needs
+ * only a small scheduling area; other combinations run the staged path and
+ * need gdn_staged_workspace_size() bytes.
+ */
+GDN_API size_t gdn_chunk_fwd_workspace_size(int64_t T_total, int H, int dk, int dv, int n_seqs,
+                                    gdn_dtype io_dtype);
+
+/*
+ * GDN prefill (forward).  Inputs q, k, v in io_dtype; log_alpha (<= 0) and
+ * beta in fp32; outputs o in io_dtype and h_T fp32.  Sections of the
+ * SparseGDN article: "Чем дорог префилл в Gated Delta Networks…" (three
+ * cost sources: intra-chunk solve, sequential chunk pass, chunk-start states)
+ * and "Селектор бюджета по парам голов и компактные снапшоты…" (outputs are
+ * produced for every token).  Chunk size 64; chunks restart at every
+ * sequence start and the last chunk of a sequence may be partial.
+ */
+GDN_API gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *log_alpha, const float *beta, const float *h0,
+                         const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
+                         int dk, int dv, gdn_dtype io_dtype, void *o, float *h_T,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Plain causal linear attention S_t = S_{t-1} + v_t k_t^T, o_t = S_t q_t
+ * ("Как ускорить LLM на длинном контексте", section "Linear attention"; the
+ * reassociated evaluation order of "За пределами self-attention", section
+ * "Линейное внимание…").  No gates, no delta term, no normaliser, causal.
+ * Same layouts and rules as gdn_chunk_fwd.
+ */
+GDN_API size_t linear_attn_fwd_workspace_size(int64_t T_total, int H, int dk, int dv, int n_seqs,
+                                      gdn_dtype io_dtype);
+GDN_API gdn_status linear_attn_fwd(const void *q, const void *k, const void *v, const float *h0,
+                           const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
+                           int dk, int dv, gdn_dtype io_dtype, void *o, float *h_T,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * One decode token of the gated delta rule for B sequences x H heads, the
+ * state updated in place: S <- a S + b (v - a S k) k^T, o = S q (the same
+ * rule as above for a single t; O(1) state per step as in "Как ускорить LLM
+ * на длинном контексте", section "Linear attention").
+ * q, k [B][H][dk], v [B][H][dv], log_alpha, beta [B][H], o [B][H][dv] are
+ * bf16; state is fp32 [B][H][dk][dv] (h = S^T), read and written once.
+ * No workspace; errors are argument errors or launch errors only.
+ */
+GDN_API gdn_status gdn_recurrent_step(const void *q, const void *k, const void *v,
+                              const void *log_alpha, const void *beta, float *state, void *o,
+                              int B, int H, int dk, int dv, void *stream);
+
+/*
+ * Staged prefill: the three chunk stages as separate kernels with their
+ * intermediates in the workspace (fp32 g, A, w, u) -- gate cumsum and
+ * decay-masked K K^T; (I + A)^-1 by forward substitution and w, u; the
+ * state pass with outputs.  Same contract as gdn_chunk_fwd /
+ * linear_attn_fwd (delta_rule = 1 / 0; log_alpha and beta are ignored and
+ * may be NULL when delta_rule = 0).  Any supported dtype and head size.
+ */
+GDN_API size_t gdn_staged_workspace_size(int64_t T_total, int H, int dk, int dv, int n_seqs,
+                                 gdn_dtype io_dtype);
+GDN_API gdn_status gdn_chunk_fwd_staged(const void *q, const void *k, const void *v,
+                                const float *log_alpha, const float *beta, const float *h0,
+                                const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
+                                int dk, int dv, gdn_dtype io_dtype, int delta_rule, void *o,
+                                float *h_T, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * The intra-chunk stages alone (SparseGDN article, "Чем дорог префилл…": the
+ * first cost source), writing their fp32 results to caller buffers:
+ *   g  [T_total][H]        running sum of log_alpha within each chunk
+ *   A  [n_chunks][H][64][64]  b_i exp(g_i - g_j) (k_i . k_j) for j < i, else 0
+ *   w  [T_total][H][dk]    (I + A)^-1 (b * exp(g) * K)
+ *   u  [T_total][H][dv]    (I + A)^-1 (b * V)
+ * where chunks are numbered sequence by sequence (n_chunks = sum over
+ * sequences of ceil(L_s / 64)); rows of A past a partial chunk's end are 0.
+ * Any of g, A may be NULL; w and u may not.  Workspace: the staged query.
+ */
+GDN_API gdn_status gdn_chunk_prepare(const void *k, const void *v, const float *log_alpha,
+                             const float *beta, const int32_t *cu_seqlens, int n_seqs,
+                             int64_t T_total, int H, int dk, int dv, gdn_dtype io_dtype,
+                             float *g, float *A, float *w, float *u, void *workspace,
+                             size_t ws_bytes, void *stream);
+
+/*
+ * Waits for `stream`, then reads the device status word of a workspace used
+ * by one of the calls above into *status (GDN_OK or a negative gdn_status).
+ */
+GDN_API gdn_status gdn_workspace_status(const void *workspace, void *stream, int *status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_B300_H */

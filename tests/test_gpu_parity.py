@@ -1,0 +1,320 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the fp64
+oracle on the same seeded inputs.
+
+Tolerance (stated for this method): max|x - x_ref| / max|x_ref| over the
+whole compared tensor, <= 1e-2 for bf16 I/O with fp32 accumulation and
+<= 1e-4 for fp32 I/O, applied separately to o and to the final state h_T.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gdn_inputs as gi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "fp32": 1e-4}
+
+
+@pytest.fixture(scope="module")
+def g():
+    import gated_deltanet_sequence_prefill_b300 as pkg
+    assert torch.cuda.is_available()
+    return pkg
+
+
+def rel(x, ref):
+    if hasattr(x, "detach"):
+        x = x.detach().double().cpu().numpy()
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.max(np.abs(x - ref)) / max(float(np.max(np.abs(ref))), 1e-30))
+
+
+def dev(inp):
+    return {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+
+
+def run_gdn(g, inp, staged=False, **kw):
+    d = dev(inp)
+    f = g.gdn_chunk_fwd_staged if staged else g.gdn_chunk_fwd
+    o, hT, ws = f(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["h0"], d["cu_seqlens"], **kw)
+    st = g.workspace_status(ws)
+    assert st == 0, g.status_string(st)
+    return o, hT
+
+
+def ref_gdn(inp, chains=None):
+    """Oracle on all chains, or on the (seq, head) pairs in `chains`."""
+    if chains is None:
+        return oracle.gdn(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"],
+                          inp["h0"], inp["cu_seqlens"])
+    cu = inp["cu_seqlens"].tolist()
+    out = {}
+    for s, h in chains:
+        a, e = cu[s], cu[s + 1]
+        h0 = None if inp["h0"] is None else inp["h0"][s:s + 1, h:h + 1]
+        o, hT = oracle.gdn(inp["q"][a:e, h:h + 1], inp["k"][a:e, h:h + 1], inp["v"][a:e, h:h + 1],
+                           inp["log_alpha"][a:e, h:h + 1], inp["beta"][a:e, h:h + 1], h0)
+        out[(s, h)] = (o[:, 0], hT[0, 0])
+    return out
+
+
+def check_chains(inp, o, hT, chains, tol):
+    ref = ref_gdn(inp, chains)
+    cu = inp["cu_seqlens"].tolist()
+    o_got = np.concatenate([o[cu[s]:cu[s + 1], h].double().cpu().numpy() for s, h in chains])
+    o_ref = np.concatenate([ref[c][0] for c in chains])
+    h_got = np.stack([hT[s, h].double().cpu().numpy() for s, h in chains])
+    h_ref = np.stack([ref[c][1] for c in chains])
+    assert rel(o_got, o_ref) <= tol, rel(o_got, o_ref)
+    assert rel(h_got, h_ref) <= tol, rel(h_got, h_ref)
+
+
+# ------------------------------------------------------------------ small / ragged
+
+def test_gdn_fp32_t256_d64(g):
+    """GDN, one sequence of 256 tokens, one head, dk = dv = 64, fp32 I/O."""
+    inp = gi.gdn_inputs([256], 1, 64, 64, "fp32", h0_std=0.0, seed=0)
+    o, hT = run_gdn(g, inp)
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["fp32"] and rel(hT, rh) <= TOL["fp32"], (rel(o, ro), rel(hT, rh))
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("staged", [False, True])
+def test_gdn_ragged_varlen(g, dk, dv, dtype, staged):
+    lengths = [1, 70, 0, 129, 64, 200, 63]
+    inp = gi.gdn_inputs(lengths, 3, dk, dv, dtype, h0_std=0.01, seed=1)
+    o, hT = run_gdn(g, inp, staged=staged)
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL[dtype], rel(o, ro)
+    assert rel(hT, rh) <= TOL[dtype], rel(hT, rh)
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_gdn_seeds(g, seed):
+    inp = gi.gdn_inputs([300, 777], 4, 128, 128, "bf16", h0_std=0.01, seed=seed)
+    o, hT = run_gdn(g, inp)
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
+
+
+def test_prepare_intermediates_match_oracle(g):
+    """Stages 1-2 alone: chunk gate sums g, A, and the WY pair w, u."""
+    lengths = [70, 129, 5]
+    inp = gi.gdn_inputs(lengths, 2, 64, 128, "fp32", h0_std=0.0, seed=3)
+    d = dev(inp)
+    n_chunks = oracle.num_chunks(inp["cu_seqlens"], 64)
+    gg, A, w, u, ws = g.gdn_chunk_prepare(d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                                          n_chunks=n_chunks)
+    assert g.workspace_status(ws) == 0
+    _, _, it = oracle.chunked(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"], None,
+                              inp["cu_seqlens"], chunk=64, intermediates=True)
+    assert rel(gg, it["g"]) <= 1e-5
+    assert rel(A, it["A"]) <= 1e-4
+    assert rel(w, it["w"]) <= 1e-4
+    assert rel(u, it["u"]) <= 1e-4
+
+
+# ------------------------------------------------------------------ workload sizes
+
+def test_linear_b2_t4096_h8(g):
+    """Plain causal linear attention, 2 x 4096 tokens, H = 8, d = 128, bf16;
+    against the token recurrence and the quadratic masked form."""
+    inp = gi.linear_inputs([4096, 4096], 8, 128, 128, "bf16", seed=0)
+    d = dev(inp)
+    o, hT, ws = g.linear_attn_fwd(d["q"], d["k"], d["v"], None, d["cu_seqlens"])
+    assert g.workspace_status(ws) == 0
+    ro, rh = oracle.linear(inp["q"], inp["k"], inp["v"], None, inp["cu_seqlens"])
+    qo, qh = oracle.linear_quadratic(inp["q"], inp["k"], inp["v"], None, inp["cu_seqlens"])
+    assert rel(ro, qo) < 1e-10
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
+    assert rel(o, qo) <= TOL["bf16"] and rel(hT, qh) <= TOL["bf16"]
+
+
+def test_linear_ragged_with_h0(g):
+    inp = gi.linear_inputs([1, 100, 0, 257], 2, 128, 128, "bf16", h0_std=0.5, seed=4)
+    d = dev(inp)
+    o, hT, ws = g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"])
+    assert g.workspace_status(ws) == 0
+    ro, rh = oracle.linear(inp["q"], inp["k"], inp["v"], inp["h0"], inp["cu_seqlens"])
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
+
+
+def test_gdn_t32768_h16(g):
+    """GDN prefill, one 32768-token sequence, H = 16, d = 128, bf16 I/O;
+    oracle on a sample of heads (every token of each)."""
+    inp = gi.gdn_inputs([32768], 16, 128, 128, "bf16", h0_std=0.01, seed=0)
+    o, hT = run_gdn(g, inp)
+    check_chains(inp, o, hT, [(0, 0), (0, 5), (0, 11), (0, 15)], TOL["bf16"])
+
+
+def test_gdn_varlen_t131072_h32(g):
+    """GDN long prefill, 4 packed sequences (seeded lengths) summing to 131072
+    tokens, H = 32, d = 128, bf16: the benchmarked call.  Oracle on 8 sampled
+    (sequence, head) chains, every token of each, and their final states."""
+    lengths = gi.varlen_lengths(131072, 4, 0)
+    inp = gi.gdn_inputs(lengths, 32, 128, 128, "bf16", h0_std=0.01, seed=0)
+    o, hT = run_gdn(g, inp)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+    check_chains(inp, o, hT, [(0, 0), (0, 31), (1, 7), (1, 20), (2, 3), (2, 16), (3, 9), (3, 30)],
+                 TOL["bf16"])
+
+
+def test_staged_matches_fused_call_t32768(g):
+    """The staged three-kernel path and gdn_chunk_fwd agree on a full-size input."""
+    inp = gi.gdn_inputs([20000, 12768], 16, 128, 128, "bf16", h0_std=0.01, seed=5)
+    o1, h1 = run_gdn(g, inp)
+    o2, h2 = run_gdn(g, inp, staged=True)
+    assert rel(o1, o2.double().cpu().numpy()) <= TOL["bf16"]
+    assert rel(h1, h2.double().cpu().numpy()) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ decode
+
+def test_decode_b128_h32(g):
+    """Decode: 128 sequences x 32 heads, d = 128, fp32 state in place.
+    The full state after 16 steps, and 8 sampled chains over 1024 steps."""
+    B, H, D = 128, 32, 128
+    state0 = gi.decode_state(B, H, D, D, seed=0)
+    state = state0.cuda()
+    chains = [(0, 0), (5, 31), (17, 3), (64, 16), (99, 8), (127, 31), (33, 12), (90, 25)]
+    ref_state = {c: state0[c[0], c[1]].double().numpy() for c in chains}
+    full_ref = state0.double().numpy()
+    steps = 1024
+    worst_o = 0.0
+    for step in range(steps):
+        inp = gi.decode_step_inputs(B, H, D, D, step, seed=0)
+        d = dev(inp)
+        o = g.gdn_recurrent_step(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], state)
+        o_cpu = o.double().cpu().numpy()
+        if step < 16:
+            ro, full_ref = oracle.decode_step(inp["q"], inp["k"], inp["v"], inp["log_alpha"],
+                                              inp["beta"], full_ref)
+            assert rel(o_cpu, ro) <= TOL["bf16"], (step, rel(o_cpu, ro))
+            if step == 15:
+                assert rel(state, full_ref) <= TOL["bf16"]
+        for (b, h) in chains:
+            ro, st = oracle.decode_step(inp["q"][b:b + 1, h:h + 1], inp["k"][b:b + 1, h:h + 1],
+                                        inp["v"][b:b + 1, h:h + 1], inp["log_alpha"][b:b + 1, h:h + 1],
+                                        inp["beta"][b:b + 1, h:h + 1],
+                                        ref_state[(b, h)][None, None])
+            ref_state[(b, h)] = st[0, 0]
+            worst_o = max(worst_o, float(np.max(np.abs(o_cpu[b, h] - ro[0, 0]))) /
+                          max(float(np.max(np.abs(ro[0, 0]))), 1e-30))
+    assert worst_o <= TOL["bf16"], worst_o
+    got = np.stack([state[b, h].double().cpu().numpy() for b, h in chains])
+    ref = np.stack([ref_state[c] for c in chains])
+    assert rel(got, ref) <= TOL["bf16"], rel(got, ref)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+def test_decode_small_heads(g, dk, dv):
+    B, H = 3, 5
+    state0 = gi.decode_state(B, H, dk, dv, seed=1)
+    state = state0.cuda()
+    ref = state0.double().numpy()
+    for step in range(5):
+        inp = gi.decode_step_inputs(B, H, dk, dv, step, seed=1)
+        d = dev(inp)
+        o = g.gdn_recurrent_step(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], state)
+        ro, ref = oracle.decode_step(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"], ref)
+        assert rel(o, ro) <= TOL["bf16"]
+    assert rel(state, ref) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_single_sequence_without_cu_seqlens(g):
+    inp = gi.gdn_inputs([333], 2, 128, 128, "bf16", h0_std=0.01, seed=6)
+    d = dev(inp)
+    o, hT, ws = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["h0"], None)
+    assert g.workspace_status(ws) == 0
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("lengths", [[1], [0, 1, 0], [64], [65], [0, 0]])
+def test_tiny_and_empty(g, lengths):
+    inp = gi.gdn_inputs(lengths, 2, 128, 128, "bf16", h0_std=0.01, seed=7)
+    o, hT = run_gdn(g, inp)
+    ro, rh = ref_gdn(inp)
+    if sum(lengths):
+        assert rel(o, ro) <= TOL["bf16"]
+    assert rel(hT, rh) <= TOL["bf16"]
+    for s, L in enumerate(lengths):  # zero-length sequences return h0 exactly
+        if L == 0:
+            assert torch.equal(hT[s].cpu(), inp["h0"][s])
+
+
+def test_no_h0_and_no_final_state(g):
+    inp = gi.gdn_inputs([100, 50], 2, 128, 128, "bf16", h0_std=0.0, seed=8)
+    d = dev(inp)
+    o, hT, ws = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], None,
+                                d["cu_seqlens"], output_final_state=False)
+    assert hT is None and g.workspace_status(ws) == 0
+    ro, _ = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["bf16"]
+
+
+def test_state_chaining_across_calls(g):
+    """h_T of a first call used as h0 of a second equals one call."""
+    inp = gi.gdn_inputs([1000], 2, 128, 128, "bf16", h0_std=0.01, seed=9)
+    d = dev(inp)
+    o, hT = run_gdn(g, inp)
+    cut = 390
+    o1, h1, _ = g.gdn_chunk_fwd(d["q"][:cut].contiguous(), d["k"][:cut].contiguous(),
+                                d["v"][:cut].contiguous(), d["log_alpha"][:cut].contiguous(),
+                                d["beta"][:cut].contiguous(), d["h0"], None)
+    o2, h2, _ = g.gdn_chunk_fwd(d["q"][cut:].contiguous(), d["k"][cut:].contiguous(),
+                                d["v"][cut:].contiguous(), d["log_alpha"][cut:].contiguous(),
+                                d["beta"][cut:].contiguous(), h1, None)
+    both = torch.cat([o1, o2]).double().cpu().numpy()
+    assert rel(o, both) <= TOL["bf16"]
+    assert rel(hT, h2.double().cpu().numpy()) <= TOL["bf16"]
+
+
+def test_outputs_written_only_in_bounds(g):
+    """Canary rows after o and h_T stay untouched (partial last chunks)."""
+    lengths = [70, 3, 129]
+    inp = gi.gdn_inputs(lengths, 2, 128, 128, "bf16", h0_std=0.01, seed=10)
+    d = dev(inp)
+    T = sum(lengths)
+    o_buf = torch.full((T + 64, 2, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    h_buf = torch.full((len(lengths) + 1, 2, 128, 128), 7.0, device="cuda")
+    o, hT, ws = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["h0"],
+                                d["cu_seqlens"], o=o_buf[:T], h_T=h_buf[:len(lengths)])
+    assert g.workspace_status(ws) == 0
+    assert bool((o_buf[T:] == 7.0).all()) and bool((h_buf[len(lengths):] == 7.0).all())
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
+
+
+def test_malformed_cu_seqlens_reported_on_device(g):
+    inp = gi.gdn_inputs([64, 64], 1, 128, 128, "bf16", h0_std=0.0, seed=11)
+    d = dev(inp)
+    for bad in ([0, 100, 64, 128], [5, 64, 128], [0, 64, 127]):
+        cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        n = len(bad) - 1
+        o = torch.zeros(128, 1, 128, dtype=torch.bfloat16, device="cuda")
+        hT = torch.zeros(n, 1, 128, 128, device="cuda")
+        _, _, ws = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], None, cu,
+                                   o=o, h_T=hT)
+        assert g.workspace_status(ws) == -4
+        _, _, ws = g.gdn_chunk_fwd_staged(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], None,
+                                          cu, o=o, h_T=hT)
+        assert g.workspace_status(ws) == -4
+
+
+def test_workspace_reused_across_calls(g):
+    a = gi.gdn_inputs([500, 20], 2, 128, 128, "bf16", h0_std=0.01, seed=12)
+    b = gi.gdn_inputs([80], 2, 128, 128, "bf16", h0_std=0.01, seed=13)
+    _, _, ws = g.gdn_chunk_fwd(*[dev(a)[k] for k in ("q", "k", "v", "log_alpha", "beta", "h0", "cu_seqlens")])
+    db = dev(b)
+    o, hT, ws2 = g.gdn_chunk_fwd(db["q"], db["k"], db["v"], db["log_alpha"], db["beta"], db["h0"],
+                                 db["cu_seqlens"], workspace=ws)
+    assert ws2 is ws and g.workspace_status(ws) == 0
+    ro, rh = ref_gdn(b)
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
