@@ -163,6 +163,36 @@ GDN_API gdn_status gdn_chunk_prepare(const void *k, const void *v, const float *
                              size_t ws_bytes, void *stream);
 
 /*
+ * Staged prefill for callers that cannot allocate device memory (no paper
+ * counterpart: this is a packaging variant of gdn_chunk_fwd_staged).  Some
+ * callers cannot call cudaMalloc -- code running inside a stream capture or
+ * a host callback, allocators that own all device memory, or plug-in hosts
+ * that hand out only input and output buffers -- so this entry point takes
+ * no workspace.  Its scratch is one fixed array of GDN_STATIC_SCRATCH_BYTES
+ * in the library's device memory; every GPU that loads the library holds it
+ * until the process exits.  The caller still passes inputs and outputs.
+ *  - Same arguments and results as gdn_chunk_fwd_staged, without workspace.
+ *  - Returns GDN_ERR_WORKSPACE, launching nothing, when the problem needs
+ *    more scratch than that (gdn_staged_workspace_size(...) bytes).
+ *  - The first call on each device looks up the array's device address
+ *    (with that device current); make that first call before any stream
+ *    capture.
+ *  - Every call shares the one array, which keeps the last call's contents;
+ *    the call re-initialises what it reads before reading it.  Calls that
+ *    overlap on the GPU (two streams, two threads) race on the array.
+ *  - device_status (device pointer, may be NULL) receives the call's device
+ *    status word (GDN_OK or GDN_ERR_SEQLENS) once the stream reaches it.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define GDN_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+GDN_API gdn_status gdn_chunk_fwd_staged_static(const void *q, const void *k, const void *v,
+                                       const float *log_alpha, const float *beta,
+                                       const float *h0, const int32_t *cu_seqlens, int n_seqs,
+                                       int64_t T_total, int H, int dk, int dv,
+                                       gdn_dtype io_dtype, int delta_rule, void *o, float *h_T,
+                                       int *device_status, void *stream);
+
+/*
  * Waits for `stream`, then reads the device status word of a workspace used
  * by one of the calls above into *status (GDN_OK or a negative gdn_status).
  */
