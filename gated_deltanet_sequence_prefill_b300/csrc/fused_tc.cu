@@ -1,10 +1,647 @@
-// fused_tc.cu -- single-kernel GDN / linear-attention prefill on tcgen05 (placeholder).
+// fused_tc.cu -- single-kernel chunked prefill of the gated delta rule and of
+// plain causal linear attention on sm_103a (bf16 I/O, dk = dv = 128, chunk 64).
+//
+// The chunk stages of the SparseGDN article ("Чем дорог префилл в Gated Delta
+// Networks…": intra-chunk delta-system solve, sequential pass over chunks,
+// outputs from chunk-start states; "Схема встраивания селектора…": the stage
+// split intra-chunk / chunk_delta_h / outputs) run inside one kernel, so no
+// intermediate (A, T, w, u, per-chunk state) ever reaches HBM: HBM sees q, k,
+// v, gates, h0 in and o, h_T out.
+//
+// One CTA owns one (sequence, head, 64-column half of the state).  The state
+// h = S^T (128 x 64 fp32 for this half) lives in registers of the four state
+// warps (one row of h per thread) for the whole sequence.  Per chunk c, with
+// g the running sum of log_alpha inside the chunk:
+//   TMA warp   : TMA q, k (2 x 64x64 boxes each), v (64 x 64), gates (64 x 4)
+//                into stage c%2; chunk-local cumsum g and the decay factors
+//   producer   : [k; q] k^T on tcgen05 (M=128 N=64 K=128) -> TMEM
+//   (4 warps)    A = beta * KK^T * exp(g_i - g_j) (strict lower), P = QK^T *
+//                exp(g_i - g_j) (causal, diagonal included)
+//                T = (I + A)^-1 (blocked forward substitution, tri_inverse.cuh)
+//                [T diag(beta e^g); T diag(beta)] x [k | v] on tcgen05
+//                -> w = T(beta e^g k) (to smem, bf16), u = T(beta v) (TMEM)
+//                q~ = q e^g and k~ = k e^{g_last - g} in place
+//   state      : D1 = [q~; w] h            (M=128 N=64 K=128)
+//   (4 warps)    v_new = u - w h           (rows 64..127 of D1, fp32 -> bf16)
+//                D2 = k~^T v_new           (M=128 N=64 K=64, A MN-major)
+//                D1[0:64] += P v_new       (M=128 N=64 K=64)
+//                h <- e^{g_last} h + D2    (fp32 registers) -> bf16 for next D1
+//                o = D1[0:64]              (bf16 store, rows < n)
+// The producer runs one chunk ahead of the state chain; TMA runs two ahead.
+// All waits are bounded; a wait that runs out sets GDN_ERR_TIMEOUT in the
+// workspace status word and the CTA unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
+#include "tc_util.cuh"
+#include "tri_inverse.cuh"
 
 namespace gdn {
 
-bool fused_supported(const PrefillArgs&) { return false; }
-cudaError_t launch_fused(const PrefillArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace fused {
+
+constexpr int kThreads = 288;  // warp 0: TMA; 1-4: producer; 5-8: state
+constexpr int kNv = 64;        // state columns per CTA
+constexpr int kD = 128;        // dk = dv
+
+// per-stage layout (bytes from the stage base)
+constexpr uint32_t kOffK0 = 0, kOffQ0 = 8192, kOffW0 = 16384;
+constexpr uint32_t kOffK1 = 24576, kOffQ1 = 32768, kOffW1 = 40960;
+constexpr uint32_t kKBlk = 24576;  // stride between the two 64-column blocks of k, q, w
+constexpr uint32_t kOffV = 49152, kOffP = 57344;
+constexpr uint32_t kOffGRaw = 65536;  // log_alpha box [64][4] then beta box [64][4]
+constexpr uint32_t kOffGate = 67584;  // derived per-token gate values (float[64] arrays)
+constexpr uint32_t kStage = 69632;
+// gate arrays (float index from kOffGate)
+constexpr int kGg = 0, kGeg = 64, kGeng = 128, kGbeg = 192, kGbb = 256, kGkdec = 320, kGscal = 384;
+// scalars at kGscal: [0] e^{g_last}, [1] safe-factor flag, [2] n valid (as float)
+
+// shared region
+constexpr uint32_t kOffTP = 2 * kStage;          // [T'; T''] 128 x 64 bf16
+constexpr uint32_t kOffHB = kOffTP + 16384;      // h bf16 [128][64]
+constexpr uint32_t kOffVN = kOffHB + 16384;      // v_new bf16 [64][64]
+constexpr uint32_t kOffAF = kOffVN + 8192;       // A / T fp32 [64][68]
+constexpr uint32_t kOffScr = kOffAF + 64 * kTriLd * 4;
+constexpr uint32_t kOffBar = kOffScr + 4 * 128 * 4;
+constexpr int kNumBars = 16;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffMisc + 64;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
+
+// barriers
+enum {
+    B_FULL = 0,     // [2] TMA bytes landed
+    B_GREADY = 2,   // [2] gate values derived
+    B_READY = 4,    // [2] producer finished chunk in stage
+    B_EMPTY = 6,    // [2] state finished with stage
+    B_UFREE = 8,    // [2] u buffer read by the state
+    B_P1 = 10, B_P2 = 11, B_M1 = 12, B_M2 = 13, B_M3 = 14, B_FIN = 15
+};
+
+// TMEM columns
+constexpr uint32_t kColD1 = 0;    // 2 x 64
+constexpr uint32_t kColD2 = 128;  // 64
+constexpr uint32_t kColP1 = 192;  // 64
+constexpr uint32_t kColW = 256;   // 128
+constexpr uint32_t kColU = 384;   // 2 x 64
+constexpr uint32_t kTmemCols = 512;
+
+constexpr uint32_t kIdP1 = tc::idesc_bf16(128, 64, false, false);
+constexpr uint32_t kIdP2w = tc::idesc_bf16(128, 128, false, true);
+constexpr uint32_t kIdP2u = tc::idesc_bf16(128, 64, false, true);
+constexpr uint32_t kId1 = tc::idesc_bf16(128, 64, false, true);
+constexpr uint32_t kId2 = tc::idesc_bf16(128, 64, true, true);
+constexpr uint32_t kId3 = tc::idesc_bf16(128, 64, false, true);
+
+struct Shared {
+    uint32_t base;  // shared-space address of the aligned base
+    char* ptr;      // generic pointer to it
+    __device__ uint32_t bar(int i) const { return base + kOffBar + 8u * i; }
+    __device__ float* gate(int s) const { return reinterpret_cast<float*>(ptr + s * kStage + kOffGate); }
+};
+
+__device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_flag) {
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+    atomicExch(&hdr->status, GDN_ERR_TIMEOUT);
+    *abort_flag = 1;
+}
+
+// decay exp(g_t - g_s) for s <= t, from per-token factors when they are safe
+__device__ __forceinline__ float decay(const float* gt, int t, int s, bool safe) {
+    return safe ? gt[kGeg + t] * gt[kGeng + s] : __expf(gt[kGg + t] - gt[kGg + s]);
+}
+
+// Scale the 128 bf16 of row r of a [64 x 128] operand (two 64-column boxes
+// kKBlk apart) by f, in place.
+__device__ __forceinline__ void scale_row(uint32_t box0, uint32_t r, float f) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t a = tc::sw128(box0 + half * kKBlk, r, j);
+            uint4 x = tc::ld_shared_v4(a);
+            float2 p0 = tc::unpack_bf16(x.x), p1 = tc::unpack_bf16(x.y);
+            float2 p2 = tc::unpack_bf16(x.z), p3 = tc::unpack_bf16(x.w);
+            tc::st_shared_v4(a, tc::pack_bf16(p0.x * f, p0.y * f), tc::pack_bf16(p1.x * f, p1.y * f),
+                             tc::pack_bf16(p2.x * f, p2.y * f), tc::pack_bf16(p3.x * f, p3.y * f));
+        }
+    }
+}
+
+// Write 64 fp32 values as one bf16 row of a 128-byte-swizzled tile.
+__device__ __forceinline__ void store_row64(uint32_t tile, uint32_t r, const float* v) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        tc::st_shared_v4(tc::sw128(tile, r, j), tc::pack_bf16(v[8 * j], v[8 * j + 1]),
+                         tc::pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                         tc::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                         tc::pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+}
+
+// Bounded mbarrier wait that also stops waiting once the CTA has aborted.
+// Every thread keeps executing the same sequence of named barriers after an
+// abort (work is skipped, barriers are not), so an abort cannot deadlock.
+struct Waiter {
+    volatile int* abort_flag;
+    char* ws;
+    __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
+        if (*abort_flag) return false;
+        if (tc::mbar_wait(bar, parity)) return true;
+        report_timeout(ws, abort_flag);
+        return false;
+    }
+};
+
+template <bool GDN>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
+               const __grid_constant__ CUtensorMap tm_b, const float* __restrict__ h0,
+               __nv_bfloat16* __restrict__ o, float* __restrict__ h_T, char* __restrict__ ws,
+               int H) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    Shared sh;
+    {
+        uintptr_t p = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+        sh.ptr = reinterpret_cast<char*>(p);
+        sh.base = tc::smem_u32(sh.ptr);
+    }
+    const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
+    if (hdr->status != GDN_OK) return;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_seqs = hdr->n_seqs;
+    PlanLayout L(n_seqs);
+    const int* cu = reinterpret_cast<const int*>(ws + L.cu);
+    const int* order = reinterpret_cast<const int*>(ws + L.order);
+    const int unit = blockIdx.x;
+    const int seq = order[unit / (2 * H)];
+    const int rem = unit % (2 * H);
+    const int head = rem >> 1, j0 = (rem & 1) * kNv;
+    const int start = cu[seq], len = cu[seq + 1] - start;
+    const int nch = (len + kChunk - 1) / kChunk;
+
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sh.ptr + kOffMisc);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sh.ptr + kOffMisc + 8);
+    const Waiter wait{abort_flag, ws};
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(sh.bar(B_FULL + s), 1);
+            tc::mbar_init(sh.bar(B_GREADY + s), 1);
+            tc::mbar_init(sh.bar(B_READY + s), 1);
+            tc::mbar_init(sh.bar(B_EMPTY + s), 1);
+            tc::mbar_init(sh.bar(B_UFREE + s), 1);
+        }
+        for (int b = B_P1; b <= B_M3; ++b) tc::mbar_init(sh.bar(b), 1);
+        tc::mbar_init(sh.bar(B_FIN), 2);
+        tc::fence_mbar_init();
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+        if (GDN) {
+            tc::prefetch_tmap(&tm_la);
+            tc::prefetch_tmap(&tm_b);
+        }
+    }
+    if (!GDN) {  // w = 0 for linear attention: zero the w boxes of both stages once
+        for (int i = tid; i < 2 * 2 * 8192 / 16; i += kThreads) {
+            const int s = i / 1024, rest = i % 1024, box = rest / 512, off = (rest % 512) * 16;
+            tc::st_shared_v4(sh.base + s * kStage + (box ? kOffW1 : kOffW0) + off, 0, 0, 0, 0);
+        }
+        tc::fence_proxy_async();
+    }
+    if (warp == 0) tc::tmem_alloc(sh.base + kOffMisc + 8, kTmemCols);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool prod_issuer = (warp == 4 && lane == 0);
+    const bool state_issuer = (warp == 6 && lane == 0);
+
+    if (warp == 0) {
+        // ================================================== TMA + gates
+        int issued = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1, u = c >> 1;
+            const uint32_t st = sh.base + s * kStage;
+            if (c >= 2) wait(sh.bar(B_EMPTY + s), (u - 1) & 1);
+            const int t0 = start + c * kChunk;
+            if (lane == 0 && !*abort_flag) {
+                const uint32_t bytes = 2 * 16384 + 8192 + (GDN ? 2048 : 0);
+                tc::mbar_arrive_expect_tx(sh.bar(B_FULL + s), bytes);
+                tc::tma_load_3d(st + kOffK0, &tm_k, 0, head, t0, sh.bar(B_FULL + s));
+                tc::tma_load_3d(st + kOffK1, &tm_k, 64, head, t0, sh.bar(B_FULL + s));
+                tc::tma_load_3d(st + kOffQ0, &tm_q, 0, head, t0, sh.bar(B_FULL + s));
+                tc::tma_load_3d(st + kOffQ1, &tm_q, 64, head, t0, sh.bar(B_FULL + s));
+                tc::tma_load_3d(st + kOffV, &tm_v, j0, head, t0, sh.bar(B_FULL + s));
+                if (GDN) {
+                    tc::tma_load_2d(st + kOffGRaw, &tm_la, head & ~3, t0, sh.bar(B_FULL + s));
+                    tc::tma_load_2d(st + kOffGRaw + 1024, &tm_b, head & ~3, t0, sh.bar(B_FULL + s));
+                }
+                issued = c + 1;
+            }
+            __syncwarp();
+            wait(sh.bar(B_FULL + s), u & 1);
+            // derived gate values of the chunk
+            const int n = min(kChunk, len - c * kChunk);
+            float* gt = sh.gate(s);
+            const float* la_raw = reinterpret_cast<const float*>(sh.ptr + s * kStage + kOffGRaw);
+            const float* b_raw = la_raw + 256;
+            const int hc = head & 3;
+            const int ta = lane, tb = lane + 32;
+            float ga = 0.f, gb = 0.f, ba, bb;
+            if (GDN) {
+                ga = ta < n ? la_raw[ta * 4 + hc] : 0.f;
+                gb = tb < n ? la_raw[tb * 4 + hc] : 0.f;
+                ba = ta < n ? b_raw[ta * 4 + hc] : 0.f;
+                bb = tb < n ? b_raw[tb * 4 + hc] : 0.f;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    float xa = __shfl_up_sync(0xffffffffu, ga, off);
+                    float xb = __shfl_up_sync(0xffffffffu, gb, off);
+                    if (lane >= off) { ga += xa; gb += xb; }
+                }
+                gb += __shfl_sync(0xffffffffu, ga, 31);
+            } else {
+                ba = ta < n ? 1.f : 0.f;
+                bb = tb < n ? 1.f : 0.f;
+            }
+            const int last = n - 1;
+            const float glast = __shfl_sync(0xffffffffu, last < 32 ? ga : gb, last & 31);
+            float amax = fmaxf(ta < n ? fabsf(ga) : 0.f, tb < n ? fabsf(gb) : 0.f);
+#pragma unroll
+            for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const float ega = __expf(ga), egb = __expf(gb);
+            gt[kGg + ta] = ga;
+            gt[kGg + tb] = gb;
+            gt[kGeg + ta] = ega;
+            gt[kGeg + tb] = egb;
+            gt[kGeng + ta] = __expf(-ga);
+            gt[kGeng + tb] = __expf(-gb);
+            gt[kGbeg + ta] = ba * ega;
+            gt[kGbeg + tb] = bb * egb;
+            gt[kGbb + ta] = ba;
+            gt[kGbb + tb] = bb;
+            gt[kGkdec + ta] = ta < n ? __expf(glast - ga) : 0.f;
+            gt[kGkdec + tb] = tb < n ? __expf(glast - gb) : 0.f;
+            if (lane == 0) {
+                gt[kGscal + 0] = __expf(glast);
+                gt[kGscal + 1] = amax <= 40.f ? 1.f : 0.f;
+                gt[kGscal + 2] = (float)n;
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(sh.bar(B_GREADY + s));
+        }
+        // after an abort, let copies already issued land before the CTA exits
+        if (lane == 0 && *abort_flag)
+            for (int c = max(0, issued - 2); c < issued; ++c)
+                tc::mbar_wait(sh.bar(B_FULL + (c & 1)), (c >> 1) & 1);
+    } else if (warp <= 4) {
+        // ================================================== producer
+        const int pw = warp - 1;                   // 0..3
+        const int r = 32 * (warp & 3) + lane;      // TMEM lane / tile row
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        float* AF = reinterpret_cast<float*>(sh.ptr + kOffAF);
+        float* scr = reinterpret_cast<float*>(sh.ptr + kOffScr);
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1, u = c >> 1;
+            const uint32_t st = sh.base + s * kStage;
+            wait(sh.bar(B_GREADY + s), u & 1);
+            const float* gt = sh.gate(s);
+            const bool safe = gt[kGscal + 1] != 0.f;
+            const int n = (int)gt[kGscal + 2];
+
+            // ---- [k; q] k^T
+            if (prod_issuer && !*abort_flag) {
+                tc::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kKBlk + (kk & 3) * 32;
+                    tc::mma_bf16(tmem + kColP1, tc::sdesc(st + kOffK0 + off, 16, 1024),
+                                 tc::sdesc(st + kOffK0 + off, 16, 1024), kIdP1, kk > 0);
+                }
+                tc::mma_commit(sh.bar(B_P1));
+            }
+            wait(sh.bar(B_P1), c & 1);
+            tc::tc_fence_after();
+            {
+                float x[64];
+                tc::tmem_ld32(tmem + lane_off + kColP1, *reinterpret_cast<float(*)[32]>(x));
+                tc::tmem_ld32(tmem + lane_off + kColP1 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+                tc::tmem_wait_ld();
+                if (r < 64) {  // row r of K K^T -> row r of A
+                    const int t = r;
+                    if (GDN) {
+                        const float bt = gt[kGbb + t];
+                        float* Ar = AF + t * kTriLd;
+#pragma unroll
+                        for (int q4 = 0; q4 < 16; ++q4) {
+                            float4 v4;
+                            float* vv = reinterpret_cast<float*>(&v4);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int sidx = 4 * q4 + e;
+                                vv[e] = (sidx < t && t < n) ? bt * x[sidx] * decay(gt, t, sidx, safe) : 0.f;
+                            }
+                            *reinterpret_cast<float4*>(Ar + 4 * q4) = v4;
+                        }
+                    }
+                } else {  // row t of Q K^T -> row t of P
+                    const int t = r - 64;
+#pragma unroll
+                    for (int sidx = 0; sidx < 64; ++sidx)
+                        x[sidx] = (sidx <= t && t < n) ? (GDN ? x[sidx] * decay(gt, t, sidx, safe) : x[sidx]) : 0.f;
+                    store_row64(st + kOffP, t, x);
+                }
+            }
+            tc::tc_fence_before();
+            tc::named_bar(1, 128);
+            // ---- T = (I + A)^-1
+            if (GDN) tri_inverse_64(AF, scr, pw, lane, 1);
+            // ---- [T diag(beta e^g); T diag(beta)] -> TP
+            {
+                const int t = r & 63;
+                const float* cs = gt + (r < 64 ? kGbeg : kGbb);
+                float x[64];
+                if (GDN) {
+                    const float* Tr = AF + t * kTriLd;
+#pragma unroll
+                    for (int sidx = 0; sidx < 64; ++sidx) x[sidx] = Tr[sidx] * cs[sidx];
+                } else {
+#pragma unroll
+                    for (int sidx = 0; sidx < 64; ++sidx) x[sidx] = sidx == t ? cs[sidx] : 0.f;
+                }
+                store_row64(sh.base + kOffTP, r, x);
+            }
+            tc::fence_proxy_async();
+            tc::named_bar(1, 128);
+            // ---- w = T' k (GDN), u = T'' v
+            if (prod_issuer) {
+                if (c >= 2) wait(sh.bar(B_UFREE + (c & 1)), ((c >> 1) - 1) & 1);
+                if (!*abort_flag) {
+                    tc::tc_fence_after();
+                    if (GDN) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_bf16(tmem + kColW, tc::sdesc(sh.base + kOffTP + kk * 32, 16, 1024),
+                                         tc::sdesc(st + kOffK0 + kk * 2048, kKBlk, 1024), kIdP2w, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_bf16(tmem + kColU + (c & 1) * 64,
+                                     tc::sdesc(sh.base + kOffTP + kk * 32, 16, 1024),
+                                     tc::sdesc(st + kOffV + kk * 2048, 8192, 1024), kIdP2u, kk > 0);
+                    tc::mma_commit(sh.bar(B_P2));
+                }
+            }
+            wait(sh.bar(B_P2), c & 1);
+            tc::tc_fence_after();
+            if (r < 64) {
+                if (GDN) {  // w row r -> bf16 into the w boxes
+                    float x[32];
+#pragma unroll
+                    for (int part = 0; part < 4; ++part) {
+                        tc::tmem_ld32(tmem + lane_off + kColW + 32 * part, x);
+                        tc::tmem_wait_ld();
+                        const uint32_t box = st + (part < 2 ? kOffW0 : kOffW1);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tc::st_shared_v4(tc::sw128(box, r, (part & 1) * 4 + j),
+                                             tc::pack_bf16(x[8 * j], x[8 * j + 1]),
+                                             tc::pack_bf16(x[8 * j + 2], x[8 * j + 3]),
+                                             tc::pack_bf16(x[8 * j + 4], x[8 * j + 5]),
+                                             tc::pack_bf16(x[8 * j + 6], x[8 * j + 7]));
+                    }
+                }
+            } else {
+                const int t = r - 64;
+                if (GDN) scale_row(st + kOffQ0, t, gt[kGeg + t]);
+                scale_row(st + kOffK0, t, gt[kGkdec + t]);
+            }
+            tc::fence_proxy_async();
+            tc::tc_fence_before();
+            tc::named_bar(1, 128);
+            if (prod_issuer) tc::mbar_arrive(sh.bar(B_READY + s));
+        }
+    } else {
+        // ================================================== state chain
+        const int r = 32 * (warp & 3) + lane;  // row of h (dk index) and TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const size_t hoff = (((size_t)seq * H + head) * kD + r) * kD + j0;
+        float h[kNv];
+        if (h0) {
+#pragma unroll
+            for (int j = 0; j < kNv; j += 4) {
+                float4 v4 = *reinterpret_cast<const float4*>(h0 + hoff + j);
+                h[j] = v4.x; h[j + 1] = v4.y; h[j + 2] = v4.z; h[j + 3] = v4.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < kNv; ++j) h[j] = 0.f;
+        }
+        store_row64(sh.base + kOffHB, r, h);
+        tc::fence_proxy_async();
+        tc::named_bar(2, 128);
+
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1, u = c >> 1, b = c & 1;
+            const uint32_t st = sh.base + s * kStage;
+            wait(sh.bar(B_READY + s), u & 1);
+            const float* gt = sh.gate(s);
+            const uint32_t d1 = tmem + kColD1 + b * 64;
+            // ---- D1 = [q~; w] h
+            if (state_issuer && !*abort_flag) {
+                tc::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma_bf16(d1, tc::sdesc(st + kOffQ0 + (kk >> 2) * kKBlk + (kk & 3) * 32, 16, 1024),
+                                 tc::sdesc(sh.base + kOffHB + kk * 2048, 8192, 1024), kId1, kk > 0);
+                tc::mma_commit(sh.bar(B_M1));
+            }
+            if (r >= 64) {
+                // ---- v_new = u - w h   (rows 64..127 of D1 are w h)
+                wait(sh.bar(B_M1), c & 1);
+                tc::tc_fence_after();
+                const int t = r - 64;
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    float wh[32], uu[32];
+                    tc::tmem_ld32(d1 + lane_off + 32 * part, wh);
+                    tc::tmem_ld32(tmem + lane_off + kColU + b * 64 + 32 * part, uu);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tc::st_shared_v4(tc::sw128(sh.base + kOffVN, t, part * 4 + j),
+                                         tc::pack_bf16(uu[8 * j] - wh[8 * j], uu[8 * j + 1] - wh[8 * j + 1]),
+                                         tc::pack_bf16(uu[8 * j + 2] - wh[8 * j + 2], uu[8 * j + 3] - wh[8 * j + 3]),
+                                         tc::pack_bf16(uu[8 * j + 4] - wh[8 * j + 4], uu[8 * j + 5] - wh[8 * j + 5]),
+                                         tc::pack_bf16(uu[8 * j + 6] - wh[8 * j + 6], uu[8 * j + 7] - wh[8 * j + 7]));
+                }
+                tc::fence_proxy_async();
+                tc::tc_fence_before();
+                tc::named_bar(3, 64);
+                if (state_issuer) {
+                    tc::mbar_arrive(sh.bar(B_UFREE + b));
+                    if (!*abort_flag) {
+                        tc::tc_fence_after();
+                        // ---- D2 = k~^T v_new
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_bf16(tmem + kColD2, tc::sdesc(st + kOffK0 + kk * 2048, kKBlk, 1024),
+                                         tc::sdesc(sh.base + kOffVN + kk * 2048, 8192, 1024), kId2, kk > 0);
+                        tc::mma_commit(sh.bar(B_M2));
+                        // ---- D1[0:64] += P v_new
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_bf16(d1, tc::sdesc(st + kOffP + kk * 32, 16, 1024),
+                                         tc::sdesc(sh.base + kOffVN + kk * 2048, 8192, 1024), kId3, 1);
+                        tc::mma_commit(sh.bar(B_M3));
+                    }
+                }
+            }
+            // ---- h <- e^{g_last} h + k~^T v_new
+            wait(sh.bar(B_M2), c & 1);
+            tc::tc_fence_after();
+            {
+                const float egl = gt[kGscal + 0];
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    float dd[32];
+                    tc::tmem_ld32(tmem + lane_off + kColD2 + 32 * part, dd);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) h[32 * part + j] = fmaf(egl, h[32 * part + j], dd[j]);
+                }
+            }
+            if (c + 1 < nch) store_row64(sh.base + kOffHB, r, h);
+            tc::fence_proxy_async();
+            tc::tc_fence_before();
+            tc::named_bar(2, 128);
+            // ---- o = rows 0..63 of D1
+            if (r < 64) {
+                wait(sh.bar(B_M3), c & 1);
+                tc::tc_fence_after();
+                const int n = min(kChunk, len - c * kChunk);
+                const int t0 = start + c * kChunk;
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    float oo[32];
+                    tc::tmem_ld32(d1 + lane_off + 32 * part, oo);
+                    tc::tmem_wait_ld();
+                    if (r < n && !*abort_flag) {
+                        uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(t0 + r) * H + head) * kD + j0 + 32 * part);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(tc::pack_bf16(oo[8 * j], oo[8 * j + 1]),
+                                                tc::pack_bf16(oo[8 * j + 2], oo[8 * j + 3]),
+                                                tc::pack_bf16(oo[8 * j + 4], oo[8 * j + 5]),
+                                                tc::pack_bf16(oo[8 * j + 6], oo[8 * j + 7]));
+                    }
+                }
+                tc::tc_fence_before();
+                if (r == 0) tc::mbar_arrive(sh.bar(B_EMPTY + s));
+            }
+        }
+        if (h_T && !*abort_flag) {
+#pragma unroll
+            for (int j = 0; j < kNv; j += 4)
+                *reinterpret_cast<float4*>(h_T + hoff + j) = make_float4(h[j], h[j + 1], h[j + 2], h[j + 3]);
+        }
+    }
+
+    // drain: both MMA issuers commit once more; wait (bounded) until every MMA
+    // of this CTA has completed before the tensor memory is released
+    if (prod_issuer || state_issuer) tc::mma_commit(sh.bar(B_FIN));
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) tc::mbar_wait(sh.bar(B_FIN), 0);
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [T][H][128] bf16, box 64 (features) x 1 (head) x 64 (tokens), 128-byte swizzle
+bool map_tokens(CUtensorMap* m, const void* ptr, int64_t T, int H) {
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+    cuuint32_t box[3] = {64, 1, 64}, es[3] = {1, 1, 1};
+    return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [T][H] fp32, box 4 (heads) x 64 (tokens)
+bool map_gates(CUtensorMap* m, const float* ptr, int64_t T, int H) {
+    cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[1] = {(cuuint64_t)H * 4};
+    cuuint32_t box[2] = {4, 64}, es[2] = {1, 1};
+    return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box,
+                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace fused
+
+bool fused_supported(const PrefillArgs& a) {
+    auto al = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
+    if (a.io != GDN_BF16 || a.dk != 128 || a.dv != 128) return false;
+    if (a.delta_rule) {
+        if (a.H % 4 != 0) return false;  // the gate boxes need H * 4 bytes to be a multiple of 16
+        if (!al(a.log_alpha, 16) || !al(a.beta, 16)) return false;
+    }
+    return al(a.q, 16) && al(a.k, 16) && al(a.v, 16) && fused::encoder() != nullptr;
+}
+
+cudaError_t launch_fused(const PrefillArgs& a, cudaStream_t st) {
+    using namespace fused;
+    const long long units = (long long)a.n_seqs * a.H * 2;
+    if (units == 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mla, mb;
+    const int64_t T = a.T_total > 0 ? a.T_total : 1;
+    // with T_total == 0 every sequence is empty and no copy is issued; the
+    // maps only need a valid address to encode
+    const void* base = a.q ? a.q : a.ws;
+    if (!map_tokens(&mq, a.q ? a.q : base, T, a.H) || !map_tokens(&mk, a.k ? a.k : base, T, a.H) ||
+        !map_tokens(&mv, a.v ? a.v : base, T, a.H))
+        return cudaErrorInvalidValue;
+    if (a.delta_rule) {
+        if (!map_gates(&mla, a.log_alpha ? a.log_alpha : (const float*)base, T, a.H) ||
+            !map_gates(&mb, a.beta ? a.beta : (const float*)base, T, a.H))
+            return cudaErrorInvalidValue;
+    } else {
+        mla = mq;
+        mb = mq;
+    }
+    auto kern = a.delta_rule ? prefill_kernel<true> : prefill_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)units, kThreads, kSmemAlloc, st>>>(mq, mk, mv, mla, mb, a.h0, (__nv_bfloat16*)a.o,
+                                                        a.h_T, a.ws, a.H);
+    return cudaGetLastError();
+}
 
 }  // namespace gdn
