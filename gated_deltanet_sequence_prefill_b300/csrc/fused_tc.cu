@@ -11,25 +11,28 @@
 // One CTA owns one (sequence, head, 64-column half of the state).  The state
 // h = S^T (128 x 64 fp32 for this half) lives in registers of the four state
 // warps (one row of h per thread) for the whole sequence.  Per chunk c, with
-// g the running sum of log_alpha inside the chunk:
-//   TMA warp   : TMA q, k (2 x 64x64 boxes each), v (64 x 64), gates (64 x 4)
-//                into stage c%2; chunk-local cumsum g and the decay factors
-//   producer   : [k; q] k^T on tcgen05 (M=128 N=64 K=128) -> TMEM
-//   (4 warps)    A = beta * KK^T * exp(g_i - g_j) (strict lower), P = QK^T *
-//                exp(g_i - g_j) (causal, diagonal included)
-//                T = (I + A)^-1 (blocked forward substitution, tri_inverse.cuh)
-//                [T diag(beta e^g); T diag(beta)] x [k | v] on tcgen05
-//                -> w = T(beta e^g k) (to smem, bf16), u = T(beta v) (TMEM)
-//                q~ = q e^g and k~ = k e^{g_last - g} in place
-//   state      : D1 = [q~; w] h            (M=128 N=64 K=128)
-//   (4 warps)    v_new = u - w h           (rows 64..127 of D1, fp32 -> bf16)
+// g the running sum of log_alpha inside the chunk, four roles run as a
+// pipeline (TMA two chunks ahead, solve one ahead of apply, apply one ahead
+// of the state chain):
+//   TMA warp     TMA q, k (2 x 64x64 boxes each), v (64 x 64), gates (64 x 4)
+//                into stage c%2 (and an L2 prefetch three chunks ahead);
+//                chunk-local cumsum g and the per-token decay factors
+//   solve (4 w)  [k; q] k^T on tcgen05 (M=128 N=64 K=128), issued one chunk
+//                ahead; A = beta KK^T exp(g_i - g_j) (strictly lower),
+//                P = QK^T exp(g_i - g_j) (causal, diagonal included);
+//                T = (I + A)^-1 (tri_inverse.cuh);
+//                [T diag(beta e^g); T diag(beta)] -> TP (bf16)
+//   apply (4 w)  TP x [k | v] on tcgen05 -> w = T(beta e^g k), u = T(beta v);
+//                w -> smem (bf16), u -> smem (bf16), q~ = q e^g and
+//                k~ = k e^{g_last - g} in place
+//   state (4 w)  D1 = [q~; w] h            (M=128 N=64 K=128)
+//                v_new = u - w h           (rows 64..127 of D1) -> bf16
 //                D2 = k~^T v_new           (M=128 N=64 K=64, A MN-major)
 //                D1[0:64] += P v_new       (M=128 N=64 K=64)
 //                h <- e^{g_last} h + D2    (fp32 registers) -> bf16 for next D1
 //                o = D1[0:64]              (bf16 store, rows < n)
-// The producer runs one chunk ahead of the state chain; TMA runs two ahead.
 // All waits are bounded; a wait that runs out sets GDN_ERR_TIMEOUT in the
-// workspace status word and the CTA unwinds.
+// workspace status word and the CTA unwinds without skipping any barrier.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -45,7 +48,7 @@ namespace gdn {
 
 namespace fused {
 
-constexpr int kThreads = 288;  // warp 0: TMA; 1-4: producer; 5-8: state
+constexpr int kThreads = 416;  // warp 0: TMA; 1-4: solve; 5-8: apply; 9-12: state
 constexpr int kNv = 64;        // state columns per CTA
 constexpr int kD = 128;        // dk = dv
 
@@ -62,13 +65,14 @@ constexpr int kGg = 0, kGeg = 64, kGeng = 128, kGbeg = 192, kGbb = 256, kGkdec =
 // scalars at kGscal: [0] e^{g_last}, [1] safe-factor flag, [2] n valid (as float)
 
 // shared region
-constexpr uint32_t kOffTP = 2 * kStage;          // [T'; T''] 128 x 64 bf16
-constexpr uint32_t kOffHB = kOffTP + 16384;      // h bf16 [128][64]
+constexpr uint32_t kOffTP = 2 * kStage;          // 2 x [T'; T''] 128 x 64 bf16
+constexpr uint32_t kOffHB = kOffTP + 2 * 16384;  // h bf16 [128][64]
 constexpr uint32_t kOffVN = kOffHB + 16384;      // v_new bf16 [64][64]
-constexpr uint32_t kOffAF = kOffVN + 8192;       // A / T fp32 [64][68]
+constexpr uint32_t kOffU = kOffVN + 8192;        // u bf16 [64][64] (swizzled rows)
+constexpr uint32_t kOffAF = kOffU + 8192;        // A / T fp32 [64][68]
 constexpr uint32_t kOffScr = kOffAF + 64 * kTriLd * 4;
 constexpr uint32_t kOffBar = kOffScr + 4 * 128 * 4;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 24;  // >= B_COUNT
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 64;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
@@ -76,20 +80,27 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // barriers
 enum {
-    B_FULL = 0,     // [2] TMA bytes landed
-    B_GREADY = 2,   // [2] gate values derived
-    B_READY = 4,    // [2] producer finished chunk in stage
-    B_EMPTY = 6,    // [2] state finished with stage
-    B_UFREE = 8,    // [2] u buffer read by the state
-    B_P1 = 10, B_P2 = 11, B_M1 = 12, B_M2 = 13, B_M3 = 14, B_FIN = 15
+    B_FULL = 0,    // [2] TMA bytes landed                      (TMA -> all)
+    B_GREADY = 2,  // [2] gate values derived                   (TMA -> solve, apply, state)
+    B_EMPTY = 4,   // [2] stage free                            (state -> TMA)
+    B_P1D = 6,     // [2] [k;q]k^T done in DP1[b]               (tcgen05 -> solve)
+    B_P1F = 20,    // [2] DP1[b] read by the solve group        (solve -> TMA warp)
+    B_TPR = 8,     // [2] TP[b] written                         (solve -> apply)
+    B_TPF = 10,    // [2] TP[b] consumed                        (apply -> solve)
+    B_READY = 12,  // [2] operands of the stage ready           (apply -> state)
+    B_P2D = 14,    // w, u MMAs done                            (tcgen05 -> apply)
+    B_UF = 15,     // u buffer read by the state                (state -> apply)
+    B_M1 = 16, B_M2 = 17, B_M3 = 18,
+    B_FIN = 19,    // every issuer's MMAs retired
+    B_COUNT = 22
 };
 
 // TMEM columns
 constexpr uint32_t kColD1 = 0;    // 2 x 64
 constexpr uint32_t kColD2 = 128;  // 64
-constexpr uint32_t kColP1 = 192;  // 64
-constexpr uint32_t kColW = 256;   // 128
-constexpr uint32_t kColU = 384;   // 2 x 64
+constexpr uint32_t kColP1 = 192;  // 2 x 64
+constexpr uint32_t kColW = 320;   // 128
+constexpr uint32_t kColU = 448;   // 64
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdP1 = tc::idesc_bf16(128, 64, false, false);
@@ -99,49 +110,10 @@ constexpr uint32_t kId1 = tc::idesc_bf16(128, 64, false, true);
 constexpr uint32_t kId2 = tc::idesc_bf16(128, 64, true, true);
 constexpr uint32_t kId3 = tc::idesc_bf16(128, 64, false, true);
 
-struct Shared {
-    uint32_t base;  // shared-space address of the aligned base
-    char* ptr;      // generic pointer to it
-    __device__ uint32_t bar(int i) const { return base + kOffBar + 8u * i; }
-    __device__ float* gate(int s) const { return reinterpret_cast<float*>(ptr + s * kStage + kOffGate); }
-};
-
 __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_flag) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     atomicExch(&hdr->status, GDN_ERR_TIMEOUT);
     *abort_flag = 1;
-}
-
-// decay exp(g_t - g_s) for s <= t, from per-token factors when they are safe
-__device__ __forceinline__ float decay(const float* gt, int t, int s, bool safe) {
-    return safe ? gt[kGeg + t] * gt[kGeng + s] : __expf(gt[kGg + t] - gt[kGg + s]);
-}
-
-// Scale the 128 bf16 of row r of a [64 x 128] operand (two 64-column boxes
-// kKBlk apart) by f, in place.
-__device__ __forceinline__ void scale_row(uint32_t box0, uint32_t r, float f) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t a = tc::sw128(box0 + half * kKBlk, r, j);
-            uint4 x = tc::ld_shared_v4(a);
-            float2 p0 = tc::unpack_bf16(x.x), p1 = tc::unpack_bf16(x.y);
-            float2 p2 = tc::unpack_bf16(x.z), p3 = tc::unpack_bf16(x.w);
-            tc::st_shared_v4(a, tc::pack_bf16(p0.x * f, p0.y * f), tc::pack_bf16(p1.x * f, p1.y * f),
-                             tc::pack_bf16(p2.x * f, p2.y * f), tc::pack_bf16(p3.x * f, p3.y * f));
-        }
-    }
-}
-
-// Write 64 fp32 values as one bf16 row of a 128-byte-swizzled tile.
-__device__ __forceinline__ void store_row64(uint32_t tile, uint32_t r, const float* v) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        tc::st_shared_v4(tc::sw128(tile, r, j), tc::pack_bf16(v[8 * j], v[8 * j + 1]),
-                         tc::pack_bf16(v[8 * j + 2], v[8 * j + 3]),
-                         tc::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                         tc::pack_bf16(v[8 * j + 6], v[8 * j + 7]));
 }
 
 // Bounded mbarrier wait that also stops waiting once the CTA has aborted.
@@ -158,6 +130,38 @@ struct Waiter {
     }
 };
 
+// Scale the 128 bf16 of row r of a [64 x 128] operand (two 64-column boxes
+// kKBlk apart) by f, in place, with packed bf16x2 multiplies (the bf16
+// product of two bf16 values is rounded once, as an fp32 multiply then a
+// rounding to bf16 would be; f itself is rounded to bf16 first).
+__device__ __forceinline__ void scale_row(uint32_t box0, uint32_t r, float f) {
+    const __nv_bfloat162 f2 = __float2bfloat162_rn(f);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t a = tc::sw128(box0 + half * kKBlk, r, j);
+            uint4 x = tc::ld_shared_v4(a);
+            __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&x);
+            p[0] = __hmul2(p[0], f2);
+            p[1] = __hmul2(p[1], f2);
+            p[2] = __hmul2(p[2], f2);
+            p[3] = __hmul2(p[3], f2);
+            tc::st_shared_v4(a, x.x, x.y, x.z, x.w);
+        }
+    }
+}
+
+// Write 64 fp32 values as one bf16 row of a 128-byte-swizzled tile.
+__device__ __forceinline__ void store_row64(uint32_t tile, uint32_t r, const float* v) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        tc::st_shared_v4(tc::sw128(tile, r, j), tc::pack_bf16(v[8 * j], v[8 * j + 1]),
+                         tc::pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                         tc::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                         tc::pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+}
+
 template <bool GDN>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -166,12 +170,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                __nv_bfloat16* __restrict__ o, float* __restrict__ h_T, char* __restrict__ ws,
                int H) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    Shared sh;
-    {
-        uintptr_t p = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
-        sh.ptr = reinterpret_cast<char*>(p);
-        sh.base = tc::smem_u32(sh.ptr);
-    }
+    // offset to the next 1024-byte boundary; pointers stay derived from the
+    // __shared__ array so every access compiles to a shared-space access
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    char* const sptr = reinterpret_cast<char*>(smem_raw) + pad;
+    const uint32_t sbase = raw + pad;
+    auto bar = [&](int i) { return sbase + kOffBar + 8u * (uint32_t)i; };
+    auto gate = [&](int s) { return reinterpret_cast<float*>(sptr + s * kStage + kOffGate); };
+
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
     if (hdr->status != GDN_OK) return;
 
@@ -187,21 +194,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int start = cu[seq], len = cu[seq + 1] - start;
     const int nch = (len + kChunk - 1) / kChunk;
 
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sh.ptr + kOffMisc);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sh.ptr + kOffMisc + 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + kOffMisc);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + kOffMisc + 8);
     const Waiter wait{abort_flag, ws};
 
     if (tid == 0) {
         *abort_flag = 0;
-        for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(sh.bar(B_FULL + s), 1);
-            tc::mbar_init(sh.bar(B_GREADY + s), 1);
-            tc::mbar_init(sh.bar(B_READY + s), 1);
-            tc::mbar_init(sh.bar(B_EMPTY + s), 1);
-            tc::mbar_init(sh.bar(B_UFREE + s), 1);
-        }
-        for (int b = B_P1; b <= B_M3; ++b) tc::mbar_init(sh.bar(b), 1);
-        tc::mbar_init(sh.bar(B_FIN), 2);
+        for (int b = 0; b < B_COUNT; ++b) tc::mbar_init(bar(b), b == B_FIN ? 4 : 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
@@ -214,46 +213,81 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (!GDN) {  // w = 0 for linear attention: zero the w boxes of both stages once
         for (int i = tid; i < 2 * 2 * 8192 / 16; i += kThreads) {
             const int s = i / 1024, rest = i % 1024, box = rest / 512, off = (rest % 512) * 16;
-            tc::st_shared_v4(sh.base + s * kStage + (box ? kOffW1 : kOffW0) + off, 0, 0, 0, 0);
+            tc::st_shared_v4(sbase + s * kStage + (box ? kOffW1 : kOffW0) + off, 0, 0, 0, 0);
         }
         tc::fence_proxy_async();
     }
-    if (warp == 0) tc::tmem_alloc(sh.base + kOffMisc + 8, kTmemCols);
+    if (warp == 0) tc::tmem_alloc(sbase + kOffMisc + 8, kTmemCols);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const bool prod_issuer = (warp == 4 && lane == 0);
-    const bool state_issuer = (warp == 6 && lane == 0);
+    const int quad = warp & 3;                        // TMEM lane quadrant of this warp
+    const int row = 32 * quad + lane;                 // TMEM lane / tile row
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    const bool tma_issuer = (warp == 0 && lane == 0);
+    const bool solve_issuer = (warp == 4 && lane == 0);
+    const bool apply_issuer = (warp == 8 && lane == 0);
+    const bool state_issuer = (warp == 10 && lane == 0);  // row 64
+
+    // ---- [k; q] k^T for chunk c into DP1[c & 1] (issued by the solve group)
+    auto issue_p1 = [&](int c) {
+        const uint32_t st = sbase + (c & 1) * kStage;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kKBlk + (kk & 3) * 32;
+            tc::mma_bf16(tmem + kColP1 + (c & 1) * 64, tc::sdesc(st + kOffK0 + off, 16, 1024),
+                         tc::sdesc(st + kOffK0 + off, 16, 1024), kIdP1, kk > 0);
+        }
+        tc::mma_commit(bar(B_P1D + (c & 1)));
+    };
 
     if (warp == 0) {
         // ================================================== TMA + gates
         int issued = 0;
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1, u = c >> 1;
-            const uint32_t st = sh.base + s * kStage;
-            if (c >= 2) wait(sh.bar(B_EMPTY + s), (u - 1) & 1);
+            const uint32_t st = sbase + s * kStage;
+            if (c >= 2) wait(bar(B_EMPTY + s), (u - 1) & 1);
             const int t0 = start + c * kChunk;
             if (lane == 0 && !*abort_flag) {
                 const uint32_t bytes = 2 * 16384 + 8192 + (GDN ? 2048 : 0);
-                tc::mbar_arrive_expect_tx(sh.bar(B_FULL + s), bytes);
-                tc::tma_load_3d(st + kOffK0, &tm_k, 0, head, t0, sh.bar(B_FULL + s));
-                tc::tma_load_3d(st + kOffK1, &tm_k, 64, head, t0, sh.bar(B_FULL + s));
-                tc::tma_load_3d(st + kOffQ0, &tm_q, 0, head, t0, sh.bar(B_FULL + s));
-                tc::tma_load_3d(st + kOffQ1, &tm_q, 64, head, t0, sh.bar(B_FULL + s));
-                tc::tma_load_3d(st + kOffV, &tm_v, j0, head, t0, sh.bar(B_FULL + s));
+                tc::mbar_arrive_expect_tx(bar(B_FULL + s), bytes);
+                tc::tma_load_3d(st + kOffK0, &tm_k, 0, head, t0, bar(B_FULL + s));
+                tc::tma_load_3d(st + kOffK1, &tm_k, 64, head, t0, bar(B_FULL + s));
+                tc::tma_load_3d(st + kOffQ0, &tm_q, 0, head, t0, bar(B_FULL + s));
+                tc::tma_load_3d(st + kOffQ1, &tm_q, 64, head, t0, bar(B_FULL + s));
+                tc::tma_load_3d(st + kOffV, &tm_v, j0, head, t0, bar(B_FULL + s));
                 if (GDN) {
-                    tc::tma_load_2d(st + kOffGRaw, &tm_la, head & ~3, t0, sh.bar(B_FULL + s));
-                    tc::tma_load_2d(st + kOffGRaw + 1024, &tm_b, head & ~3, t0, sh.bar(B_FULL + s));
+                    tc::tma_load_2d(st + kOffGRaw, &tm_la, head & ~3, t0, bar(B_FULL + s));
+                    tc::tma_load_2d(st + kOffGRaw + 1024, &tm_b, head & ~3, t0, bar(B_FULL + s));
                 }
                 issued = c + 1;
+                if (c + 3 < nch) {  // warm L2 for a later chunk; its copy then waits less
+                    const int tp = t0 + 3 * kChunk;
+                    tc::tma_prefetch_3d(&tm_k, 0, head, tp);
+                    tc::tma_prefetch_3d(&tm_k, 64, head, tp);
+                    tc::tma_prefetch_3d(&tm_q, 0, head, tp);
+                    tc::tma_prefetch_3d(&tm_q, 64, head, tp);
+                    tc::tma_prefetch_3d(&tm_v, j0, head, tp);
+                    if (GDN) {
+                        tc::tma_prefetch_2d(&tm_la, head & ~3, tp);
+                        tc::tma_prefetch_2d(&tm_b, head & ~3, tp);
+                    }
+                }
             }
             __syncwarp();
-            wait(sh.bar(B_FULL + s), u & 1);
+            wait(bar(B_FULL + s), u & 1);
+            // [k; q] k^T of this chunk, once the solve group has released DP1[c & 1]
+            if (tma_issuer) {
+                if (c >= 2) wait(bar(B_P1F + (c & 1)), ((c >> 1) - 1) & 1);
+                if (!*abort_flag) issue_p1(c);
+            }
             // derived gate values of the chunk
             const int n = min(kChunk, len - c * kChunk);
-            float* gt = sh.gate(s);
-            const float* la_raw = reinterpret_cast<const float*>(sh.ptr + s * kStage + kOffGRaw);
+            float* gt = gate(s);
+            const float* la_raw = reinterpret_cast<const float*>(sptr + s * kStage + kOffGRaw);
             const float* b_raw = la_raw + 256;
             const int hc = head & 3;
             const int ta = lane, tb = lane + 32;
@@ -298,143 +332,165 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 gt[kGscal + 2] = (float)n;
             }
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(sh.bar(B_GREADY + s));
+            if (lane == 0) tc::mbar_arrive(bar(B_GREADY + s));
         }
         // after an abort, let copies already issued land before the CTA exits
         if (lane == 0 && *abort_flag)
             for (int c = max(0, issued - 2); c < issued; ++c)
-                tc::mbar_wait(sh.bar(B_FULL + (c & 1)), (c >> 1) & 1);
+                tc::mbar_wait(bar(B_FULL + (c & 1)), (c >> 1) & 1);
     } else if (warp <= 4) {
-        // ================================================== producer
-        const int pw = warp - 1;                   // 0..3
-        const int r = 32 * (warp & 3) + lane;      // TMEM lane / tile row
-        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        float* AF = reinterpret_cast<float*>(sh.ptr + kOffAF);
-        float* scr = reinterpret_cast<float*>(sh.ptr + kOffScr);
+        // ================================================== solve group
+        const int pw = warp - 1;  // 0..3
+        float* AF = reinterpret_cast<float*>(sptr + kOffAF);
+        float* scr = reinterpret_cast<float*>(sptr + kOffScr);
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1, u = c >> 1;
-            const uint32_t st = sh.base + s * kStage;
-            wait(sh.bar(B_GREADY + s), u & 1);
-            const float* gt = sh.gate(s);
+            const uint32_t st = sbase + s * kStage;
+            wait(bar(B_GREADY + s), u & 1);
+            wait(bar(B_P1D + (c & 1)), u & 1);
+            tc::tc_fence_after();
+            const float* gt = gate(s);
             const bool safe = gt[kGscal + 1] != 0.f;
             const int n = (int)gt[kGscal + 2];
-
-            // ---- [k; q] k^T
-            if (prod_issuer && !*abort_flag) {
-                tc::tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kKBlk + (kk & 3) * 32;
-                    tc::mma_bf16(tmem + kColP1, tc::sdesc(st + kOffK0 + off, 16, 1024),
-                                 tc::sdesc(st + kOffK0 + off, 16, 1024), kIdP1, kk > 0);
-                }
-                tc::mma_commit(sh.bar(B_P1));
-            }
-            wait(sh.bar(B_P1), c & 1);
-            tc::tc_fence_after();
+            float x[64];
+            tc::tmem_ld32(tmem + lane_off + kColP1 + (c & 1) * 64, *reinterpret_cast<float(*)[32]>(x));
+            tc::tmem_ld32(tmem + lane_off + kColP1 + (c & 1) * 64 + 32,
+                          *reinterpret_cast<float(*)[32]>(x + 32));
+            tc::tmem_wait_ld();
+            tc::tc_fence_before();
+            tc::named_bar(1, 128);  // DP1[c & 1] fully read
+            if (solve_issuer) tc::mbar_arrive(bar(B_P1F + (c & 1)));
+            // rows 0..63: K K^T -> A (fp32); rows 64..127: Q K^T -> P (bf16 tile)
             {
-                float x[64];
-                tc::tmem_ld32(tmem + lane_off + kColP1, *reinterpret_cast<float(*)[32]>(x));
-                tc::tmem_ld32(tmem + lane_off + kColP1 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-                tc::tmem_wait_ld();
-                if (r < 64) {  // row r of K K^T -> row r of A
-                    const int t = r;
-                    if (GDN) {
-                        const float bt = gt[kGbb + t];
-                        float* Ar = AF + t * kTriLd;
+                const int t = row & 63;
+                const bool is_a = row < 64;
+                if (!is_a || GDN) {
+                    const float rs = (is_a ? gt[kGbb + t] : 1.f) * gt[kGeg + t];
+                    const int lim = is_a ? t : t + 1;  // s < lim kept
+                    const bool tok = t < n;
+                    if (safe) {
 #pragma unroll
                         for (int q4 = 0; q4 < 16; ++q4) {
-                            float4 v4;
-                            float* vv = reinterpret_cast<float*>(&v4);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int sidx = 4 * q4 + e;
-                                vv[e] = (sidx < t && t < n) ? bt * x[sidx] * decay(gt, t, sidx, safe) : 0.f;
-                            }
-                            *reinterpret_cast<float4*>(Ar + 4 * q4) = v4;
+                            const float4 en = *reinterpret_cast<const float4*>(gt + kGeng + 4 * q4);
+                            const int s0 = 4 * q4;
+                            x[s0 + 0] = (tok && s0 + 0 < lim) ? x[s0 + 0] * en.x * rs : 0.f;
+                            x[s0 + 1] = (tok && s0 + 1 < lim) ? x[s0 + 1] * en.y * rs : 0.f;
+                            x[s0 + 2] = (tok && s0 + 2 < lim) ? x[s0 + 2] * en.z * rs : 0.f;
+                            x[s0 + 3] = (tok && s0 + 3 < lim) ? x[s0 + 3] * en.w * rs : 0.f;
                         }
+                    } else {
+                        const float gtt = gt[kGg + t], bsc = is_a ? gt[kGbb + t] : 1.f;
+#pragma unroll
+                        for (int sidx = 0; sidx < 64; ++sidx)
+                            x[sidx] = (tok && sidx < lim) ? x[sidx] * bsc * __expf(gtt - gt[kGg + sidx]) : 0.f;
                     }
-                } else {  // row t of Q K^T -> row t of P
-                    const int t = r - 64;
+                    if (is_a) {
+                        float* Ar = AF + t * kTriLd;
 #pragma unroll
-                    for (int sidx = 0; sidx < 64; ++sidx)
-                        x[sidx] = (sidx <= t && t < n) ? (GDN ? x[sidx] * decay(gt, t, sidx, safe) : x[sidx]) : 0.f;
-                    store_row64(st + kOffP, t, x);
+                        for (int q4 = 0; q4 < 16; ++q4)
+                            *reinterpret_cast<float4*>(Ar + 4 * q4) =
+                                make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+                    } else {
+                        store_row64(st + kOffP, t, x);
+                    }
                 }
-            }
-            tc::tc_fence_before();
-            tc::named_bar(1, 128);
-            // ---- T = (I + A)^-1
-            if (GDN) tri_inverse_64(AF, scr, pw, lane, 1);
-            // ---- [T diag(beta e^g); T diag(beta)] -> TP
-            {
-                const int t = r & 63;
-                const float* cs = gt + (r < 64 ? kGbeg : kGbb);
-                float x[64];
-                if (GDN) {
-                    const float* Tr = AF + t * kTriLd;
-#pragma unroll
-                    for (int sidx = 0; sidx < 64; ++sidx) x[sidx] = Tr[sidx] * cs[sidx];
-                } else {
-#pragma unroll
-                    for (int sidx = 0; sidx < 64; ++sidx) x[sidx] = sidx == t ? cs[sidx] : 0.f;
-                }
-                store_row64(sh.base + kOffTP, r, x);
             }
             tc::fence_proxy_async();
             tc::named_bar(1, 128);
-            // ---- w = T' k (GDN), u = T'' v
-            if (prod_issuer) {
-                if (c >= 2) wait(sh.bar(B_UFREE + (c & 1)), ((c >> 1) - 1) & 1);
-                if (!*abort_flag) {
-                    tc::tc_fence_after();
-                    if (GDN) {
+            if (GDN) tri_inverse_64(AF, scr, pw, lane, 1);
+            // ---- TP[c & 1]: rows 0..63 T diag(beta e^g), rows 64..127 T diag(beta)
+            if (c >= 2) wait(bar(B_TPF + (c & 1)), ((c >> 1) - 1) & 1);
+            {
+                const int t = row & 63;
+                const float* cs = gt + (row < 64 ? kGbeg : kGbb);
+                const uint32_t tp = sbase + kOffTP + (c & 1) * 16384;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc::mma_bf16(tmem + kColW, tc::sdesc(sh.base + kOffTP + kk * 32, 16, 1024),
-                                         tc::sdesc(st + kOffK0 + kk * 2048, kKBlk, 1024), kIdP2w, kk > 0);
+                for (int jb = 0; jb < 4; ++jb) {
+                    float v16[16];
+                    if (GDN && jb <= (t >> 4)) {
+                        const float* Tr = tri_block_row(AF, t, jb);
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            const float4 tv = *reinterpret_cast<const float4*>(Tr + e);
+                            const float4 sv = *reinterpret_cast<const float4*>(cs + 16 * jb + e);
+                            v16[e] = tv.x * sv.x; v16[e + 1] = tv.y * sv.y;
+                            v16[e + 2] = tv.z * sv.z; v16[e + 3] = tv.w * sv.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v16[e] = (!GDN && 16 * jb + e == t) ? cs[t] : 0.f;
                     }
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2)
+                        tc::st_shared_v4(tc::sw128(tp, row, 2 * jb + h2),
+                                         tc::pack_bf16(v16[8 * h2], v16[8 * h2 + 1]),
+                                         tc::pack_bf16(v16[8 * h2 + 2], v16[8 * h2 + 3]),
+                                         tc::pack_bf16(v16[8 * h2 + 4], v16[8 * h2 + 5]),
+                                         tc::pack_bf16(v16[8 * h2 + 6], v16[8 * h2 + 7]));
+                }
+            }
+            tc::fence_proxy_async();
+            tc::named_bar(1, 128);
+            if (solve_issuer) tc::mbar_arrive(bar(B_TPR + (c & 1)));
+        }
+    } else if (warp <= 8) {
+        // ================================================== apply group
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1, u = c >> 1;
+            const uint32_t st = sbase + s * kStage;
+            const uint32_t tp = sbase + kOffTP + (c & 1) * 16384;
+            wait(bar(B_GREADY + s), u & 1);
+            wait(bar(B_TPR + (c & 1)), u & 1);
+            // ---- w = T' k (GDN), u = T'' v
+            if (apply_issuer && !*abort_flag) {
+                tc::tc_fence_after();
+                if (GDN) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_bf16(tmem + kColU + (c & 1) * 64,
-                                     tc::sdesc(sh.base + kOffTP + kk * 32, 16, 1024),
-                                     tc::sdesc(st + kOffV + kk * 2048, 8192, 1024), kIdP2u, kk > 0);
-                    tc::mma_commit(sh.bar(B_P2));
+                        tc::mma_bf16(tmem + kColW, tc::sdesc(tp + kk * 32, 16, 1024),
+                                     tc::sdesc(st + kOffK0 + kk * 2048, kKBlk, 1024), kIdP2w, kk > 0);
                 }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_bf16(tmem + kColU, tc::sdesc(tp + kk * 32, 16, 1024),
+                                 tc::sdesc(st + kOffV + kk * 2048, 8192, 1024), kIdP2u, kk > 0);
+                tc::mma_commit(bar(B_P2D));
             }
-            wait(sh.bar(B_P2), c & 1);
+            wait(bar(B_P2D), c & 1);
             tc::tc_fence_after();
-            if (r < 64) {
-                if (GDN) {  // w row r -> bf16 into the w boxes
-                    float x[32];
+            if (apply_issuer) tc::mbar_arrive(bar(B_TPF + (c & 1)));
+            const float* gt = gate(s);
+            if (row < 64) {
+                if (GDN) {  // w row -> bf16 into the w boxes
 #pragma unroll
-                    for (int part = 0; part < 4; ++part) {
-                        tc::tmem_ld32(tmem + lane_off + kColW + 32 * part, x);
+                    for (int half = 0; half < 2; ++half) {
+                        float x[64];
+                        tc::tmem_ld32(tmem + lane_off + kColW + 64 * half, *reinterpret_cast<float(*)[32]>(x));
+                        tc::tmem_ld32(tmem + lane_off + kColW + 64 * half + 32,
+                                      *reinterpret_cast<float(*)[32]>(x + 32));
                         tc::tmem_wait_ld();
-                        const uint32_t box = st + (part < 2 ? kOffW0 : kOffW1);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tc::st_shared_v4(tc::sw128(box, r, (part & 1) * 4 + j),
-                                             tc::pack_bf16(x[8 * j], x[8 * j + 1]),
-                                             tc::pack_bf16(x[8 * j + 2], x[8 * j + 3]),
-                                             tc::pack_bf16(x[8 * j + 4], x[8 * j + 5]),
-                                             tc::pack_bf16(x[8 * j + 6], x[8 * j + 7]));
+                        store_row64(st + (half ? kOffW1 : kOffW0), row, x);
                     }
                 }
+                scale_row(st + kOffK0, row, gt[kGkdec + row]);
             } else {
-                const int t = r - 64;
+                const int t = row - 64;
+                if (c >= 1) wait(bar(B_UF), (c - 1) & 1);
+                float x[64];
+                tc::tmem_ld32(tmem + lane_off + kColU, *reinterpret_cast<float(*)[32]>(x));
+                tc::tmem_ld32(tmem + lane_off + kColU + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+                tc::tmem_wait_ld();
+                store_row64(sbase + kOffU, t, x);
                 if (GDN) scale_row(st + kOffQ0, t, gt[kGeg + t]);
-                scale_row(st + kOffK0, t, gt[kGkdec + t]);
             }
             tc::fence_proxy_async();
             tc::tc_fence_before();
-            tc::named_bar(1, 128);
-            if (prod_issuer) tc::mbar_arrive(sh.bar(B_READY + s));
+            tc::named_bar(2, 128);
+            if (apply_issuer) tc::mbar_arrive(bar(B_READY + s));
         }
     } else {
         // ================================================== state chain
-        const int r = 32 * (warp & 3) + lane;  // row of h (dk index) and TMEM lane
-        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const int r = row;  // row of h (dk index) and TMEM lane
         const size_t hoff = (((size_t)seq * H + head) * kD + r) * kD + j0;
         float h[kNv];
         if (h0) {
@@ -447,15 +503,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
             for (int j = 0; j < kNv; ++j) h[j] = 0.f;
         }
-        store_row64(sh.base + kOffHB, r, h);
+        store_row64(sbase + kOffHB, r, h);
         tc::fence_proxy_async();
-        tc::named_bar(2, 128);
+        tc::named_bar(3, 128);
 
         for (int c = 0; c < nch; ++c) {
             const int s = c & 1, u = c >> 1, b = c & 1;
-            const uint32_t st = sh.base + s * kStage;
-            wait(sh.bar(B_READY + s), u & 1);
-            const float* gt = sh.gate(s);
+            const uint32_t st = sbase + s * kStage;
+            wait(bar(B_READY + s), u & 1);
+            const float* gt = gate(s);
             const uint32_t d1 = tmem + kColD1 + b * 64;
             // ---- D1 = [q~; w] h
             if (state_issuer && !*abort_flag) {
@@ -463,52 +519,55 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc::mma_bf16(d1, tc::sdesc(st + kOffQ0 + (kk >> 2) * kKBlk + (kk & 3) * 32, 16, 1024),
-                                 tc::sdesc(sh.base + kOffHB + kk * 2048, 8192, 1024), kId1, kk > 0);
-                tc::mma_commit(sh.bar(B_M1));
+                                 tc::sdesc(sbase + kOffHB + kk * 2048, 8192, 1024), kId1, kk > 0);
+                tc::mma_commit(bar(B_M1));
             }
             if (r >= 64) {
                 // ---- v_new = u - w h   (rows 64..127 of D1 are w h)
-                wait(sh.bar(B_M1), c & 1);
+                wait(bar(B_M1), c & 1);
                 tc::tc_fence_after();
                 const int t = r - 64;
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    float wh[32], uu[32];
-                    tc::tmem_ld32(d1 + lane_off + 32 * part, wh);
-                    tc::tmem_ld32(tmem + lane_off + kColU + b * 64 + 32 * part, uu);
+                for (int part = 0; part < 4; ++part) {
+                    float wh[16];
+                    tc::tmem_ld16(d1 + lane_off + 16 * part, wh);
+                    const uint4 ua = tc::ld_shared_v4(tc::sw128(sbase + kOffU, t, 2 * part));
+                    const uint4 ub = tc::ld_shared_v4(tc::sw128(sbase + kOffU, t, 2 * part + 1));
                     tc::tmem_wait_ld();
+                    const uint32_t uw[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        tc::st_shared_v4(tc::sw128(sh.base + kOffVN, t, part * 4 + j),
-                                         tc::pack_bf16(uu[8 * j] - wh[8 * j], uu[8 * j + 1] - wh[8 * j + 1]),
-                                         tc::pack_bf16(uu[8 * j + 2] - wh[8 * j + 2], uu[8 * j + 3] - wh[8 * j + 3]),
-                                         tc::pack_bf16(uu[8 * j + 4] - wh[8 * j + 4], uu[8 * j + 5] - wh[8 * j + 5]),
-                                         tc::pack_bf16(uu[8 * j + 6] - wh[8 * j + 6], uu[8 * j + 7] - wh[8 * j + 7]));
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 uu = tc::unpack_bf16(uw[e]);
+                        pk[e] = tc::pack_bf16(uu.x - wh[2 * e], uu.y - wh[2 * e + 1]);
+                    }
+                    tc::st_shared_v4(tc::sw128(sbase + kOffVN, t, 2 * part), pk[0], pk[1], pk[2], pk[3]);
+                    tc::st_shared_v4(tc::sw128(sbase + kOffVN, t, 2 * part + 1), pk[4], pk[5], pk[6], pk[7]);
                 }
                 tc::fence_proxy_async();
                 tc::tc_fence_before();
-                tc::named_bar(3, 64);
+                tc::named_bar(4, 64);
                 if (state_issuer) {
-                    tc::mbar_arrive(sh.bar(B_UFREE + b));
+                    tc::mbar_arrive(bar(B_UF));
                     if (!*abort_flag) {
                         tc::tc_fence_after();
                         // ---- D2 = k~^T v_new
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc::mma_bf16(tmem + kColD2, tc::sdesc(st + kOffK0 + kk * 2048, kKBlk, 1024),
-                                         tc::sdesc(sh.base + kOffVN + kk * 2048, 8192, 1024), kId2, kk > 0);
-                        tc::mma_commit(sh.bar(B_M2));
+                                         tc::sdesc(sbase + kOffVN + kk * 2048, 8192, 1024), kId2, kk > 0);
+                        tc::mma_commit(bar(B_M2));
                         // ---- D1[0:64] += P v_new
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc::mma_bf16(d1, tc::sdesc(st + kOffP + kk * 32, 16, 1024),
-                                         tc::sdesc(sh.base + kOffVN + kk * 2048, 8192, 1024), kId3, 1);
-                        tc::mma_commit(sh.bar(B_M3));
+                                         tc::sdesc(sbase + kOffVN + kk * 2048, 8192, 1024), kId3, 1);
+                        tc::mma_commit(bar(B_M3));
                     }
                 }
             }
             // ---- h <- e^{g_last} h + k~^T v_new
-            wait(sh.bar(B_M2), c & 1);
+            wait(bar(B_M2), c & 1);
             tc::tc_fence_after();
             {
                 const float egl = gt[kGscal + 0];
@@ -521,14 +580,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     for (int j = 0; j < 32; ++j) h[32 * part + j] = fmaf(egl, h[32 * part + j], dd[j]);
                 }
             }
-            if (c + 1 < nch) store_row64(sh.base + kOffHB, r, h);
+            if (c + 1 < nch) store_row64(sbase + kOffHB, r, h);
             tc::fence_proxy_async();
             tc::tc_fence_before();
-            tc::named_bar(2, 128);
+            tc::named_bar(3, 128);
             // ---- o = rows 0..63 of D1
             if (r < 64) {
-                wait(sh.bar(B_M3), c & 1);
+                wait(bar(B_M3), c & 1);
                 tc::tc_fence_after();
+                if (r == 0) tc::mbar_arrive(bar(B_EMPTY + s));  // every MMA reading the stage has retired
                 const int n = min(kChunk, len - c * kChunk);
                 const int t0 = start + c * kChunk;
 #pragma unroll
@@ -547,7 +607,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
                 tc::tc_fence_before();
-                if (r == 0) tc::mbar_arrive(sh.bar(B_EMPTY + s));
             }
         }
         if (h_T && !*abort_flag) {
@@ -557,12 +616,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     }
 
-    // drain: both MMA issuers commit once more; wait (bounded) until every MMA
-    // of this CTA has completed before the tensor memory is released
-    if (prod_issuer || state_issuer) tc::mma_commit(sh.bar(B_FIN));
+    // drain: every MMA issuer commits once more; wait (bounded) until every
+    // MMA of this CTA has completed before the tensor memory is released
+    if (tma_issuer || solve_issuer || apply_issuer || state_issuer) tc::mma_commit(bar(B_FIN));
     tc::tc_fence_before();
     __syncthreads();
-    if (tid == 0) tc::mbar_wait(sh.bar(B_FIN), 0);
+    if (tid == 0) tc::mbar_wait(bar(B_FIN), 0);
     __syncthreads();
     tc::tc_fence_after();
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
