@@ -6,6 +6,8 @@ H = 32 heads, dk = dv = 128, bf16 q/k/v/o, fp32 gates and states, chunk 64
 larger than L2 (4.35 GB), so no L2 flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --workload {gdn_t32768_h16, gdn_t131072_h32_single, linear_b2_t4096_h8,
+                              decode_b128_h32}     (the other workloads, one GPU)
 
 One JSON line is printed by rank 0.  Under torchrun each rank runs the same
 per-GPU workload on its own GPU (weak scaling, no collective on the data
@@ -76,6 +78,9 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()  # make sure sampling runs before the timed region starts
+            while not self.lines and time.time() - t0 < 5.0:
+                time.sleep(0.02)
         except OSError:
             self.proc = None
         return self
@@ -85,6 +90,7 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        time.sleep(0.25)  # at least a couple of samples from the end of the timed region
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -316,6 +322,101 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+def run_workload(args):
+    """Time one of the other workloads on one GPU (same timing rules)."""
+    import torch
+    import gated_deltanet_sequence_prefill_b300 as g
+    torch.cuda.set_device(0)
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+    flush = None
+    name = args.workload
+    if name == "decode_b128_h32":
+        B, Hh, Dd, steps = 128, 32, 128, 1024
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(0)
+        state = (torch.randn(B, Hh, Dd, Dd, generator=gen, device="cuda") * 0.01).float()
+
+        def step_inputs():
+            q = torch.randn(B, Hh, Dd, generator=gen, device="cuda")
+            k = torch.randn(B, Hh, Dd, generator=gen, device="cuda")
+            q = (q / q.norm(dim=-1, keepdim=True)).bfloat16()
+            k = (k / k.norm(dim=-1, keepdim=True)).bfloat16()
+            v = torch.randn(B, Hh, Dd, generator=gen, device="cuda").bfloat16()
+            la = (-torch.nn.functional.softplus(torch.randn(B, Hh, generator=gen, device="cuda")) * 0.1).bfloat16()
+            be = torch.sigmoid(torch.randn(B, Hh, generator=gen, device="cuda")).bfloat16()
+            return q, k, v, la, be
+        inputs = [step_inputs() for _ in range(steps)]
+        o = torch.empty(B, Hh, Dd, dtype=torch.bfloat16, device="cuda")
+
+        def run():
+            for q, k, v, la, be in inputs:
+                g.gdn_recurrent_step(q, k, v, la, be, state, o=o)
+        units, unit = B * steps, "tokens/s"
+        bytes_per_call = steps * (2 * B * Hh * Dd * Dd * 4 + 4 * B * Hh * Dd * 2 + 2 * B * Hh * 2)
+        launches = steps
+        cfg = {"workload": name, "B": B, "H": Hh, "dk": Dd, "dv": Dd, "steps_per_call": steps,
+               "l2": "state 537 MB per step, larger than L2, no flush"}
+    else:
+        if name == "linear_b2_t4096_h8":
+            lengths, Hh, kind = [4096, 4096], 8, "linear"
+            inp = gi.linear_inputs(lengths, Hh, D, D, "bf16", seed=0)
+            flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        elif name == "gdn_t32768_h16":
+            lengths, Hh, kind = [32768], 16, "gdn"
+            inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
+        elif name == "gdn_t131072_h32_single":
+            lengths, Hh, kind = [131072], 32, "gdn"
+            inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
+        else:
+            raise SystemExit("unknown workload " + name)
+        d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+        Tt, nn = sum(lengths), len(lengths)
+        o = torch.empty(Tt, Hh, D, dtype=torch.bfloat16, device="cuda")
+        hT = torch.empty(nn, Hh, D, D, dtype=torch.float32, device="cuda")
+        wsz = g.chunk_fwd_workspace_size(Tt, Hh, D, D, nn, delta_rule=(kind == "gdn"))
+        ws = torch.empty(max(wsz, 256), dtype=torch.uint8, device="cuda")
+        if kind == "gdn":
+            def run():
+                g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["h0"],
+                                d["cu_seqlens"], o=o, h_T=hT, workspace=ws)
+        else:
+            def run():
+                g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"], o=o, h_T=hT,
+                                  workspace=ws)
+        units, unit = Tt, "tokens/s"
+        bytes_per_call = 4 * Tt * Hh * D * 2 + (2 * Tt * Hh * 4 if kind == "gdn" else 0) + \
+            (2 if kind == "gdn" else 1) * nn * Hh * D * D * 4
+        launches = 2
+        cfg = {"workload": name, "T": Tt, "H": Hh, "dk": D, "dv": D, "seq_lens": lengths,
+               "chunk": 64, "l2": ("L2 flushed (256 MB write) between timed calls"
+                                   if flush is not None else "inputs larger than L2, no flush")}
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    times = []
+    with ClockSampler(0) as clk:
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    achieved = bytes_per_call / (ms / 1e3) / 1e9
+    line = {"metric": name + " throughput", "value": units / (ms / 1e3), "unit": unit, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic (seeded)", "config": cfg,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm"], "traffic": None, "peak_source": pk["src"],
+                         "alg_bytes_per_call": bytes_per_call},
+            "gpu_launches": launches * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -323,7 +424,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=None)
     args = ap.parse_args()
+    if args.workload:
+        run_workload(args)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
