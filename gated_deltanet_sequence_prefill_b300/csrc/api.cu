@@ -76,14 +76,15 @@ PrefillArgs make_args(const void* q, const void* k, const void* v, const float* 
 }
 
 gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
-    const bool fused = fused_supported(a);
+    const bool pair = pair_supported(a);
+    const bool fused = pair || fused_supported(a);
     size_t need = plan_bytes(a.n_seqs);
     if (!fused) need += staged_intermediate_bytes(a.T_total, a.H, a.dk, a.dv, a.n_seqs);
     gdn_status s = check_prefill(a, ws_bytes, need, true);
     if (s != GDN_OK) return s;
     if (!fused) return run_staged(a, st, nullptr, nullptr, nullptr, nullptr, true);
     cudaError_t e = launch_plan(a.cu_seqlens, a.n_seqs, a.T_total, a.ws, st);
-    if (e == cudaSuccess) e = launch_fused(a, st);
+    if (e == cudaSuccess) e = pair ? launch_pair(a, st) : launch_fused(a, st);
     return cuda_status(e);
 }
 

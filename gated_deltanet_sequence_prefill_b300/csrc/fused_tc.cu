@@ -664,6 +664,10 @@ bool map_gates(CUtensorMap* m, const float* ptr, int64_t T, int H) {
 
 }  // namespace fused
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return fused::encoder(); }
+bool encode_token_map(CUtensorMap* m, const void* p, int64_t T, int H) { return fused::map_tokens(m, p, T, H); }
+bool encode_gate_map(CUtensorMap* m, const float* p, int64_t T, int H) { return fused::map_gates(m, p, T, H); }
+
 bool fused_supported(const PrefillArgs& a) {
     auto al = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
     if (a.io != GDN_BF16 || a.dk != 128 || a.dv != 128) return false;

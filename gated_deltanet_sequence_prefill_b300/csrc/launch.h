@@ -47,8 +47,14 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const voi
                           const void* beta, float* state, void* o, int B, int H, int dk, int dv,
                           cudaStream_t st);
 
-// Fused single-kernel prefill (bf16, dk = dv = 128): tcgen05 + TMA.
+// Fused single-kernel prefill (bf16, dk = dv = 128): tcgen05 + TMA, one SM
+// per (sequence, head, 64-column half of the state).
 bool fused_supported(const PrefillArgs& a);
 cudaError_t launch_fused(const PrefillArgs& a, cudaStream_t st);
+
+// Fused prefill on a 2-CTA cluster per (sequence, head): solve on one SM,
+// state pass on the other (bf16, dk = dv = 128).
+bool pair_supported(const PrefillArgs& a);
+cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t st);
 
 }  // namespace gdn
