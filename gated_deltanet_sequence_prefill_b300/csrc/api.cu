@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of libgdn_b300.so (declared in gdn.h):
 // host-side argument checks, workspace carving and kernel launches.
 #include <cuda_runtime.h>
+#include <stdlib.h>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -75,8 +76,16 @@ PrefillArgs make_args(const void* q, const void* k, const void* v, const float* 
     return a;
 }
 
+// The 2-SM cluster kernel (solve and state pass on separate SMs) is the
+// default; GDN_PREFILL_SINGLE_SM=1 in the environment selects the single-SM
+// kernel (one CTA per sequence, head and 64-column half of the state).
+bool single_sm_requested() {
+    const char* e = getenv("GDN_PREFILL_SINGLE_SM");
+    return e != nullptr && e[0] == '1';
+}
+
 gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
-    const bool pair = pair_supported(a);
+    const bool pair = !single_sm_requested() && pair_supported(a);
     const bool fused = pair || fused_supported(a);
     size_t need = plan_bytes(a.n_seqs);
     if (!fused) need += staged_intermediate_bytes(a.T_total, a.H, a.dk, a.dv, a.n_seqs);

@@ -6,32 +6,35 @@
 // Networks…": intra-chunk delta-system solve, sequential pass over chunks,
 // outputs from chunk-start states) are split across the two SMs of the pair
 // so that the long-latency solve never holds the buffers the sequential
-// state pass needs:
+// state pass needs.  The state pass works on the transpose S = h^T (dv x dk),
+// so that S and v_new are tensor-core A operands held in TMEM:
 //
-//  front CTA (rank 0): the delta-system solve, one chunk ahead or more
+//  front CTA (rank 0): the delta-system solve, up to three chunks ahead
 //    TMA warp   q, k (2 x 64x64 SW128 boxes each) and the gates of the head
 //               into a 3-stage ring; chunk-local cumsum g and decay factors;
 //               [k; q] k^T on tcgen05 (M=128 N=64 K=128) into TMEM
 //    3 solve warpgroups, chunk c on group c % 3 (one per ring stage):
 //               A = beta KK^T exp(g_i - g_j) (strictly lower),
-//               P = QK^T exp(g_i - g_j) (causal, diagonal included),
+//               P^ = QK^T e^{-g_last} (causal; QK^T exp(g_i - g_j) when the
+//                    chunk's decay range is large),
 //               T = (I + A)^-1 (tri_inverse.cuh),
-//               P staged locally; once the back has armed the chunk's slot,
-//               P (64x64 bf16) and [T diag(beta e^g) | 0 | T diag(beta)] are
-//               pushed into the back CTA's shared memory with st.async
+//               w^T = k^T (T diag(beta e^g))^T on tcgen05,
+//               then -w (as [dk][t]), P^ and T diag(beta) are pushed into the
+//               back CTA's shared memory with st.async
 //  back CTA (rank 1): everything that touches the state
-//    TMA warp   k, q, v (both 64-column halves) and the gates into a 2-slot
-//               ring; the gate factors the back needs
-//    apply      w = T diag(beta e^g) k  -> TMEM, then -w (bf16) into the slot
-//               u = T diag(beta) v      -> written by the MMA straight into
-//                                          rows 64..127 of the chain's D1
-//               q~ = q e^g, k~ = k e^{g_last - g} (in place)
-//    chain      8 warps; h = S^T (128 x 128 fp32) in registers, each thread
-//               one row and one 64-column half
-//               D1 += [q~; -w] h        (M=128 N=128 K=128, accumulating onto
-//                                        [0; u]: rows 64..127 become v_new)
-//               v_new -> bf16 smem; D2 = k~^T v_new; D1[0:64] += P v_new
-//               h <- e^{g_last} h + D2; o = D1[0:64]
+//    TMA warp   q, k into a 3-entry ring, v and the gates into a 2-entry ring;
+//               the gate factors the back needs
+//    chain      8 warps, each thread one row j of S and one 64-column half;
+//               S in TMEM twice: fp32 (the accumulator of D2) and bf16 (the
+//               A operand)
+//               D1v  = u^T = v^T (T diag(beta))^T, then += S (-w)^T: v_new^T
+//               D1o  = S q^T
+//               v^ = e^{g_last - g} v_new (bf16, TMEM)
+//               S <- e^{g_last} S (fp32, in place), then S += v^^T k on the
+//               tensor core;  D1o += v^^T P^^T
+//    output     4 warps: o = e^{g} D1o, staged in the dead k tile and written
+//               with a TMA store
+//    MMA warp   issues every MMA of the back, warp-converged (lane 0 issues)
 //
 // HBM sees q, k, v, gates, h0 in and o, h_T out; q and k are read by both
 // CTAs (the second read is an L2 hit).  All waits are bounded; a wait that
@@ -54,7 +57,7 @@ bool encode_gate_map(CUtensorMap* m, const float* ptr, int64_t T, int H);
 
 namespace pair {
 
-constexpr int kThreads = 416;  // 13 warps in both CTAs
+constexpr int kThreads = 448;  // 14 warps in both CTAs
 constexpr int kD = 128;
 
 // ---------------------------------------------------------------- front layout
@@ -64,31 +67,36 @@ constexpr uint32_t kFGRaw = 32768;                                        // la 
 constexpr uint32_t kFGate = 34816;                                        // derived gate arrays
 constexpr uint32_t kFStage = 36864;
 constexpr int kFGroups = 3;                                // = ring stages: chunk c uses both c % 3
-constexpr uint32_t kFPst = kFGroups * kFStage;             // 3 x P staging (bf16 64x64, swizzled)
-constexpr uint32_t kFAF = kFPst + kFGroups * 8192;         // 3 x A/T fp32 [64][68]
+constexpr uint32_t kFPst = kFGroups * kFStage;             // 3 x P^ staging (bf16 64x64, swizzled)
+constexpr uint32_t kFT1 = kFPst + kFGroups * 8192;         // 3 x T' (bf16 64x64, K-major B operand)
+constexpr uint32_t kFAF = kFT1 + kFGroups * 8192;          // 3 x A/T fp32 [64][68]
 constexpr uint32_t kFScr = kFAF + kFGroups * 64 * kTriLd * 4;  // 3 x 4 x 128 floats
 constexpr uint32_t kFBar = kFScr + kFGroups * 4 * 128 * 4;
 constexpr uint32_t kFEnd = kFBar + 32 * 8 + 64;
 
 // ---------------------------------------------------------------- back layout
-constexpr uint32_t kBK0 = 0, kBQ0 = 8192, kBW0 = 16384, kBK1 = 24576, kBQ1 = 32768, kBW1 = 40960;
-constexpr uint32_t kBBlk = 24576;  // stride between the two 64-column blocks of k, q, w
-constexpr uint32_t kBV0 = 49152, kBV1 = 57344, kBP = 65536;
-constexpr uint32_t kBGRaw = 73728, kBGate = 75776;
-constexpr uint32_t kBSlot = 77824;
-constexpr uint32_t kBTP = 2 * kBSlot;            // [T' | 0 | T''], 3 x 8 KB
-constexpr uint32_t kBHB = kBTP + 3 * 8192;       // h bf16 [128][128]: two 64-column blocks
-constexpr uint32_t kBVN = kBHB + 2 * 16384;      // v_new bf16 [64][128]: two 64-column blocks
-constexpr uint32_t kBBar = kBVN + 2 * 8192;
+// Chain ring (3 entries, chunk c in entry c % 3): q and k as two 64-column
+// SW128 boxes each (the k tile later stages o), -w as [128 i][64 t] (the
+// MN-major B operand of the w MMA), P^, the derived gate values.
+constexpr uint32_t kBBox = 8192;  // stride between the two 64-column boxes
+constexpr uint32_t kCQ = 0, kCK = 16384, kCW = 32768, kCP = 49152, kCGate = 57344;
+constexpr uint32_t kCEntry = 59392;
+// Apply ring (2 entries, chunk c in entry c % 2): v (two boxes), T'' pushed
+// by the front, the raw log-decay of four heads.
+constexpr uint32_t kARing = 3 * kCEntry;
+constexpr uint32_t kAV = 0, kAT2 = 16384, kALa = 24576;
+constexpr uint32_t kAEntry = 25600;
+constexpr uint32_t kBBar = kARing + 2 * kAEntry;
 constexpr uint32_t kBEnd = kBBar + 32 * 8 + 64;
 
 constexpr uint32_t kSmemBytes = (kFEnd > kBEnd ? kFEnd : kBEnd);
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 static_assert(kFBar + 32 * 8 <= kSmemBytes && kBBar + 32 * 8 <= kSmemBytes, "barriers");
+static_assert(kCEntry % 1024 == 0 && kARing % 1024 == 0 && kAEntry % 1024 == 0, "tile alignment");
 
 // gate arrays (float index from the gate area); scalars at kGscal:
-// [0] e^{g_last}, [1] safe-factor flag, [2] n valid
+// [0] e^{g_last}, [1] safe-factor flag, [2] n valid, [3] e^{-g_last}
 constexpr int kGg = 0, kGeg = 64, kGeng = 128, kGbeg = 192, kGbb = 256, kGkdec = 320, kGscal = 384;
 
 // ---------------------------------------------------------------- barriers
@@ -99,45 +107,56 @@ enum {
     F_EMPTY = 6,    // [3] stage free
     F_P1D = 9,      // [3] [k;q]k^T done in DP1[group]
     F_P1F = 12,     // [3] DP1[group] read
-    F_ARMED = 15,   // [2] back slot armed for this use   (remote arrive by the back)
-    F_TPF = 17,     // TP buffer consumed by the back      (remote arrive by the back)
+    F_ARMED = 15,   // [3] back chain entry armed for this chunk  (remote arrive by the back)
     F_PUSHED = 18,  // [3] group pushed its chunk (orders the pushes of the three groups)
-    F_FIN = 21,
-    F_COUNT = 22
+    F_WD = 21,      // [3] w^T MMA of the group done
+    F_FIN = 24,
+    F_COUNT = 25
 };
 // back
 enum {
-    B_FULLT = 0,    // [2] own TMA landed
-    B_FULLP = 2,    // [2] P and TP pushed by the front
-    B_GREADY = 4,   // [2] gate values derived
-    B_SLOTFREE = 6, // [2] the chain is done with the slot
-    B_D1F = 8,      // [2] D1[b] read by the output epilogue (count 4 warps)
-    B_P2D = 10,     // w / u MMAs done
-    B_READY = 11,   // [2] slot operands ready for the chain
-    B_M1 = 13,      // [q~; -w] h done
-    B_M2 = 14,      // k~^T v_new done
-    B_M3 = 15,      // P v_new done
-    B_FIN = 16,
-    B_COUNT = 17
+    B_FULLC = 0,    // [3] q, k landed in the chain entry
+    B_FULLA = 3,    // [2] v, log-decay landed in the apply entry
+    B_FULLP = 5,    // [3] -w, P^, T'' pushed by the front (counted on the chain entry)
+    B_GREADY = 8,   // [3] gate values derived into the chain entry
+    B_CFREE = 11,   // [3] chain entry free (o store has read its staging)
+    B_AFREE = 14,   // [2] apply entry free (u MMA done)
+    B_D1OF = 16,    // [2] D1o[b] read by the output warps
+    B_M3 = 18,      // [2] D1o[b] complete
+    B_M1W = 20,     // D1v = v_new^T
+    B_M2 = 21,      // S += v^^T k done
+    B_SREADY = 22,  // S (bf16) of the next chunk in TMEM (chain -> issuer)
+    B_VREADY = 23,  // v^ in TMEM (chain -> issuer)
+    B_FIN = 24,
+    B_COUNT = 25
 };
 
 // TMEM columns
 constexpr uint32_t kFColP1 = 0;        // front: 3 x 64
-constexpr uint32_t kFTmemCols = 256;
-constexpr uint32_t kBColW = 0;         // back: w 128
-constexpr uint32_t kBColD1 = 128;      // back: D1 2 x 128
-constexpr uint32_t kBColD2 = 384;      // back: D2 128
+constexpr uint32_t kFColW = 256;       // front: 3 x 64, w^T (lane = dk row i)
+constexpr uint32_t kFTmemCols = 512;
+// back (lane = dv row j of the state)
+constexpr uint32_t kTD1o = 0;          // 2 x 64: o^T accumulators (fp32)
+constexpr uint32_t kTD1v = 128;        // 2 x 64: u^T - S w^T = v_new^T (fp32)
+constexpr uint32_t kTD2 = 256;         // S (fp32), 128 cols: S += v^^T k accumulates here
+constexpr uint32_t kTS = 384;          // S (bf16 pairs), 64 cols: A operand
+constexpr uint32_t kTVN = 448;         // v^ (bf16 pairs), 32 cols: A operand
 constexpr uint32_t kBTmemCols = 512;
 
 constexpr uint32_t kIdP1 = tc::idesc_bf16(128, 64, false, false);
-constexpr uint32_t kIdP2w = tc::idesc_bf16(128, 128, false, true);
-constexpr uint32_t kIdP2u = tc::idesc_bf16(128, 128, false, true);
-constexpr uint32_t kId1 = tc::idesc_bf16(128, 128, false, true);
-constexpr uint32_t kId2 = tc::idesc_bf16(128, 128, true, true);
-constexpr uint32_t kId3 = tc::idesc_bf16(128, 128, false, true);
+constexpr uint32_t kIdWU = tc::idesc_bf16(128, 64, true, false);   // A = k^T / v^T (MN-major), B = T (K-major)
+constexpr uint32_t kId1w = tc::idesc_bf16(128, 64, false, true);   // A = S (TMEM), B = -w [i][t]
+constexpr uint32_t kId1q = tc::idesc_bf16(128, 64, false, false);  // A = S (TMEM), B = q [t][i]
+constexpr uint32_t kId2 = tc::idesc_bf16(128, 128, false, true);   // A = v^T (TMEM), B = k [t][i]
+constexpr uint32_t kId3 = tc::idesc_bf16(128, 64, false, false);   // A = v^T (TMEM), B = P^ [t][s]
 
-__device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_flag) {
-    atomicExch(&reinterpret_cast<WsHeader*>(ws)->status, GDN_ERR_TIMEOUT);
+// A wait that ran out: GDN_ERR_TIMEOUT in the status word, and the first
+// barrier that gave up (1000 + index on the solve CTA, 2000 + index on the
+// state CTA) in the header's first spare word, for diagnosis.
+__device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_flag, int site) {
+    WsHeader* h = reinterpret_cast<WsHeader*>(ws);
+    atomicExch(&h->status, GDN_ERR_TIMEOUT);
+    atomicCAS(&h->pad[0], 0, site);
     *abort_flag = 1;
 }
 
@@ -146,16 +165,18 @@ __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_fla
 struct Waiter {
     volatile int* abort_flag;
     char* ws;
+    uint32_t bar_base;
+    int site_base;
     __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
         if (*abort_flag) return false;
         if (tc::mbar_wait(bar, parity)) return true;
-        report_timeout(ws, abort_flag);
+        report_timeout(ws, abort_flag, site_base + (int)((bar - bar_base) >> 3));
         return false;
     }
     __device__ __forceinline__ bool remote(uint32_t bar, uint32_t parity) const {
         if (*abort_flag) return false;
         if (tc::mbar_wait_cluster(bar, parity)) return true;
-        report_timeout(ws, abort_flag);
+        report_timeout(ws, abort_flag, site_base + (int)((bar - bar_base) >> 3));
         return false;
     }
 };
@@ -177,33 +198,8 @@ __device__ __forceinline__ void store_row64_neg(uint32_t tile, uint32_t r, const
                          tc::pack_bf16(-v[8 * j + 4], -v[8 * j + 5]),
                          tc::pack_bf16(-v[8 * j + 6], -v[8 * j + 7]));
 }
-// The same row, written into another CTA's tile with st.async.
-__device__ __forceinline__ void push_row64(uint32_t remote_tile, uint32_t r, const float* v,
-                                           uint32_t remote_bar) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        tc::st_async_v4(tc::sw128(remote_tile, r, j), tc::pack_bf16(v[8 * j], v[8 * j + 1]),
-                        tc::pack_bf16(v[8 * j + 2], v[8 * j + 3]),
-                        tc::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                        tc::pack_bf16(v[8 * j + 6], v[8 * j + 7]), remote_bar);
-}
-
-__device__ __forceinline__ void scale_row(uint32_t box0, uint32_t r, float f) {
-    const __nv_bfloat162 f2 = __float2bfloat162_rn(f);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t a = tc::sw128(box0 + half * kBBlk, r, j);
-            uint4 x = tc::ld_shared_v4(a);
-            __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&x);
-            p[0] = __hmul2(p[0], f2);
-            p[1] = __hmul2(p[1], f2);
-            p[2] = __hmul2(p[2], f2);
-            p[3] = __hmul2(p[3], f2);
-            tc::st_shared_v4(a, x.x, x.y, x.z, x.w);
-        }
-    }
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
 // Per-token gate values of a chunk (one warp): running sum g of log_alpha
@@ -252,6 +248,7 @@ __device__ __forceinline__ void derive_gates(const float* la_raw, const float* b
         gt[kGscal + 0] = __expf(glast);
         gt[kGscal + 1] = amax <= 40.f ? 1.f : 0.f;
         gt[kGscal + 2] = (float)n;
+        gt[kGscal + 3] = __expf(-glast);
     }
     __syncwarp();
 }
@@ -260,8 +257,9 @@ template <bool GDN>
 __global__ void __launch_bounds__(kThreads, 1)
 pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
-            const __grid_constant__ CUtensorMap tm_b, const float* __restrict__ h0,
-            __nv_bfloat16* __restrict__ o, float* __restrict__ h_T, char* __restrict__ ws, int H) {
+            const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_o,
+            const float* __restrict__ h0, __nv_bfloat16* __restrict__ o, float* __restrict__ h_T,
+            char* __restrict__ ws, int H) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -269,73 +267,67 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t sbase = raw + pad;  // identical in both CTAs (same kernel, same layout)
 
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
-    const bool dead = hdr->status != GDN_OK;  // uniform across the cluster
+    // loaded values are broadcast from lane 0 so that the compiler treats them,
+    // and the loops over chunks they bound, as warp-uniform
+    const bool dead = __shfl_sync(0xffffffffu, hdr->status, 0) != GDN_OK;  // uniform across the cluster
 
     const uint32_t rank = tc::cluster_rank();
     const bool front = rank == 0;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the warp index and the TMEM base are broadcast from lane 0 so that the
+    // compiler sees them as warp-uniform: role branches then stay in uniform
+    // control flow and MMA descriptors are built in uniform registers
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
     const int n_seqs = hdr->n_seqs;
     PlanLayout L(n_seqs);
     const int* cu = reinterpret_cast<const int*>(ws + L.cu);
     const int* order = reinterpret_cast<const int*>(ws + L.order);
     const int unit = blockIdx.x >> 1;
-    const int seq = dead ? 0 : order[unit / H];
+    const int seq = dead ? 0 : __shfl_sync(0xffffffffu, order[unit / H], 0);
     const int head = unit % H;
-    const int start = dead ? 0 : cu[seq];
-    const int len = dead ? 0 : cu[seq + 1] - start;
+    const int start = dead ? 0 : __shfl_sync(0xffffffffu, cu[seq], 0);
+    const int len = dead ? 0 : __shfl_sync(0xffffffffu, cu[seq + 1], 0) - start;
     const int nch = (len + kChunk - 1) / kChunk;
 
     const uint32_t bar_base = sbase + (front ? kFBar : kBBar);
     auto bar = [&](int i) { return bar_base + 8u * (uint32_t)i; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + (front ? kFBar : kBBar) + 32 * 8);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (front ? kFBar : kBBar) + 32 * 8 + 8);
-    const Waiter wait{abort_flag, ws};
+    const Waiter wait{abort_flag, ws, bar_base, front ? 1000 : 2000};
 
     if (tid == 0) {
         *abort_flag = 0;
         if (front) {
             for (int b = 0; b < F_COUNT; ++b) tc::mbar_init(bar(b), b == F_FIN ? 4 : 1);
         } else {
-            for (int b = 0; b < B_COUNT; ++b) {
-                uint32_t cnt = 1;
-                if (b == B_D1F || b == B_D1F + 1) cnt = 4;
-                if (b == B_FIN) cnt = 2;
-                tc::mbar_init(bar(b), cnt);
-            }
+            for (int b = 0; b < B_COUNT; ++b) tc::mbar_init(bar(b), 1);
         }
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
-        if (!front) tc::prefetch_tmap(&tm_v);
+        if (!front) {
+            tc::prefetch_tmap(&tm_v);
+            tc::prefetch_tmap(&tm_o);
+        }
         if (GDN) {
             tc::prefetch_tmap(&tm_la);
             tc::prefetch_tmap(&tm_b);
         }
     }
-    if (!front) {
-        // the zero block between T' and T'' (the rows 0..63 of the u MMA's A operand),
-        // and w = 0 for linear attention
-        for (int i = tid; i < 8192 / 16; i += kThreads) tc::st_shared_v4(sbase + kBTP + 8192 + 16 * i, 0, 0, 0, 0);
-        if (!GDN)
-            for (int i = tid; i < 2 * 2 * 8192 / 16; i += kThreads) {
-                const int s = i / 1024, rest = i % 1024, box = rest / 512, off = (rest % 512) * 16;
-                tc::st_shared_v4(sbase + s * kBSlot + (box ? kBW1 : kBW0) + off, 0, 0, 0, 0);
-            }
-        tc::fence_proxy_async();
-    }
+    __syncwarp();  // lane-0-only work above: reconverge before any .aligned instruction
     if (warp == 0) tc::tmem_alloc(sbase + (front ? kFBar : kBBar) + 32 * 8 + 8, front ? kFTmemCols : kBTmemCols);
     tc::tc_fence_before();
     __syncthreads();
     tc::cluster_sync();  // both CTAs' barriers exist before any remote access
     tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
     const int quad = warp & 3;
     const int row = 32 * quad + lane;
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
 
-    // peer addresses (front -> back)
-    const uint32_t peer_base = tc::map_to_rank(sbase, 1);
-    const uint32_t peer_bar_b = peer_base + kBBar;  // back barrier array, as seen from the front
+    // peer addresses
+    const uint32_t peer_base = tc::map_to_rank(sbase, 1);           // back smem, seen from the front
+    const uint32_t peer_bar_b = peer_base + kBBar;
     const uint32_t peer_bar_f = tc::map_to_rank(sbase + kFBar, 0);  // front barriers, seen from the back
 
     const bool issuer0 = (warp == 0 && lane == 0);
@@ -375,29 +367,26 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
                 __syncwarp();
                 wait(bar(F_FULL + f), uf & 1);
-                if (lane == 0) {
-                    if (c >= kFGroups) wait(bar(F_P1F + f), (uf - 1) & 1);
-                    if (!*abort_flag) {
-                        tc::tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t off = (kk >> 2) * kFBlk + (kk & 3) * 32;
-                            tc::mma_bf16(tmem + kFColP1 + f * 64, tc::sdesc(st + kFK0 + off, 16, 1024),
-                                         tc::sdesc(st + kFK0 + off, 16, 1024), kIdP1, kk > 0);
-                        }
-                        tc::mma_commit(bar(F_P1D + f));
-                    }
+                if (c >= kFGroups) wait(bar(F_P1F + f), (uf - 1) & 1);
+                if (!*abort_flag) {
+                    tc::tc_fence_after();
+                    const uint64_t d0 = tc::sdesc(st + kFK0, 16, 1024), d1 = tc::sdesc(st + kFK0 + kFBlk, 16, 1024);
+                    tc::mma_batch_ss(lane == 0, tmem + kFColP1 + f * 64, d0, 2, d0, 2, kIdP1, 4, false);
+                    tc::mma_batch_ss(lane == 0, tmem + kFColP1 + f * 64, d1, 2, d1, 2, kIdP1, 4, true);
+                    tc::mma_commit_p(lane == 0, bar(F_P1D + f));
                 }
                 const float* la_raw = reinterpret_cast<const float*>(sptr + f * kFStage + kFGRaw);
                 derive_gates<GDN>(la_raw, la_raw + 256, head & 3, min(kChunk, len - c * kChunk),
                                   reinterpret_cast<float*>(sptr + f * kFStage + kFGate), lane);
                 if (lane == 0) tc::mbar_arrive(bar(F_GREADY + f));
+                __syncwarp();
             }
             if (lane == 0 && *abort_flag)
                 for (int c = max(0, issued - kFGroups); c < issued; ++c)
                     tc::mbar_wait(bar(F_FULL + c % kFGroups), (c / kFGroups) & 1);
             if (issuer0) tc::mma_commit(bar(F_FIN));
-        } else {
+            __syncwarp();
+        } else if (warp <= 12) {
             // ---- solve groups: group g takes chunks c with c % 3 == g
             const int grp = (warp - 1) >> 2;  // 0, 1, 2
             const int pw = (warp - 1) & 3;    // warp within the group
@@ -406,30 +395,41 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             float* AF = reinterpret_cast<float*>(sptr + kFAF + grp * 64 * kTriLd * 4);
             float* scr = reinterpret_cast<float*>(sptr + kFScr + grp * 4 * 128 * 4);
             const uint32_t pst = sbase + kFPst + grp * 8192;
+            const uint32_t t1s = sbase + kFT1 + grp * 8192;
+            const uint32_t stg = sbase + grp * kFStage;
             for (int c = grp; c < nch && !dead; c += kFGroups) {
-                const int uf = c / kFGroups, s = c & 1, us = c >> 1;
+                const int uf = c / kFGroups, e = c % 3, a = c & 1;
                 wait(bar(F_GREADY + grp), uf & 1);
                 wait(bar(F_P1D + grp), uf & 1);
+                __syncwarp();
                 tc::tc_fence_after();
                 const float* gt = reinterpret_cast<const float*>(sptr + grp * kFStage + kFGate);
                 const bool safe = gt[kGscal + 1] != 0.f;
                 const int n = (int)gt[kGscal + 2];
-                float x[64];
-                tc::tmem_ld32(tmem + lane_off + kFColP1 + grp * 64, *reinterpret_cast<float(*)[32]>(x));
-                tc::tmem_ld32(tmem + lane_off + kFColP1 + grp * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-                tc::tmem_wait_ld();
-                tc::tc_fence_before();
-                tc::named_bar(nb, 128);
-                if (gissuer) tc::mbar_arrive(bar(F_P1F + grp));
-                // rows 0..63: K K^T -> A (fp32); rows 64..127: Q K^T -> P (staged, bf16)
+                const int t = row & 63;
                 {
-                    const int t = row & 63;
+                    float x[64];
+                    tc::tmem_ld32(tmem + lane_off + kFColP1 + grp * 64, *reinterpret_cast<float(*)[32]>(x));
+                    tc::tmem_ld32(tmem + lane_off + kFColP1 + grp * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+                    tc::tmem_wait_ld();
+                    tc::tc_fence_before();
+                    tc::named_bar(nb, 128);
+                    if (gissuer) tc::mbar_arrive(bar(F_P1F + grp));
+                    __syncwarp();
+                    // rows 0..63: K K^T -> A (fp32); rows 64..127: Q K^T -> P^ (staged, bf16).
+                    // When the chunk's decay range is moderate, P^ = (q k^T)_causal e^{-g_last};
+                    // the back then scales v_new by e^{g_last - g} and o by e^{g}, which gives
+                    // the same o and h.
                     const bool is_a = row < 64;
                     if (!is_a || GDN) {
                         const float rs = (is_a ? gt[kGbb + t] : 1.f) * gt[kGeg + t];
                         const int lim = is_a ? t : t + 1;
                         const bool tok = t < n;
-                        if (safe) {
+                        if (safe && !is_a) {
+                            const float eml = gt[kGscal + 3];
+#pragma unroll
+                            for (int sidx = 0; sidx < 64; ++sidx) x[sidx] = (tok && sidx < lim) ? x[sidx] * eml : 0.f;
+                        } else if (safe) {
 #pragma unroll
                             for (int q4 = 0; q4 < 16; ++q4) {
                                 const float4 en = *reinterpret_cast<const float4*>(gt + kGeng + 4 * q4);
@@ -457,86 +457,129 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     }
                 }
                 tc::named_bar(nb, 128);
-                if (GDN) tri_inverse_64(AF, scr, pw, lane, nb);
-                // ---- push P and [T diag(beta e^g) | 0 | T diag(beta)] in chunk order, once
-                // the back has consumed the previous TP and armed this chunk's slot (the
-                // pushed bytes are counted on that slot's barrier).  Waiting for chunk
-                // c - 1's push first keeps every parity wait below at most one phase behind.
-                if (c >= 1) {
-                    wait(bar(F_PUSHED + (c - 1) % kFGroups), ((c - 1) / kFGroups) & 1);
-                    wait.remote(bar(F_TPF), (c - 1) & 1);
+                // row t of T diag(cs): T from the inverse (GDN), the identity otherwise
+                auto t_row = [&](const float* cs, float (&v)[64]) {
+#pragma unroll
+                    for (int jb = 0; jb < 4; ++jb) {
+                        if (GDN && jb <= (t >> 4)) {
+                            const float* Tr = tri_block_row(AF, t, jb);
+#pragma unroll
+                            for (int e4 = 0; e4 < 16; e4 += 4) {
+                                const float4 tv = *reinterpret_cast<const float4*>(Tr + e4);
+                                const float4 sv = *reinterpret_cast<const float4*>(cs + 16 * jb + e4);
+                                v[16 * jb + e4] = tv.x * sv.x;
+                                v[16 * jb + e4 + 1] = tv.y * sv.y;
+                                v[16 * jb + e4 + 2] = tv.z * sv.z;
+                                v[16 * jb + e4 + 3] = tv.w * sv.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e4 = 0; e4 < 16; ++e4) v[16 * jb + e4] = (!GDN && 16 * jb + e4 == t) ? cs[t] : 0.f;
+                        }
+                    }
+                };
+                if (GDN) {
+                    tri_inverse_64(AF, scr, pw, lane, nb);
+                    // T' = T diag(beta e^g) (bf16, K-major) for w^T = k^T T'^T on this SM
+                    if (row < 64) {
+                        float v[64];
+                        t_row(gt + kGbeg, v);
+                        store_row64(t1s, t, v);
+                    }
+                    tc::fence_proxy_async();
+                    tc::tc_fence_before();
+                    tc::named_bar(nb, 128);
+                    if (pw == 3 && !*abort_flag) {
+                        tc::tc_fence_after();
+                        tc::mma_batch_ss(lane == 0, tmem + kFColW + 64 * grp, tc::sdesc(stg + kFK0, kFBlk, 1024), 128,
+                                         tc::sdesc(t1s, 16, 1024), 2, kIdWU, 4, false);
+                        tc::mma_commit_p(lane == 0, bar(F_WD + grp));
+                    }
+                    __syncwarp();
                 }
-                wait.remote(bar(F_ARMED + s), us & 1);
+                // ---- push -w, P^ (chain entry c % 3) and T'' = T diag(beta) (apply entry
+                // c % 2) in chunk order, once the back has armed them (the bytes are counted
+                // on the chain entry's barrier).  Waiting for chunk c - 1's push first keeps
+                // the parity wait below at most one phase behind.
+                if (c >= 1) wait(bar(F_PUSHED + (c - 1) % kFGroups), ((c - 1) / kFGroups) & 1);
+                wait.remote(bar(F_ARMED + e), (c / 3) & 1);
                 if (!*abort_flag) {
-                    const int t = row & 63;
-                    const uint32_t fb = peer_bar_b + 8u * (B_FULLP + s);
+                    const uint32_t fb = peer_bar_b + 8u * (B_FULLP + e);
+                    const uint32_t centry = peer_base + e * kCEntry;
                     if (row >= 64) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const uint4 pv = tc::ld_shared_v4(tc::sw128(pst, t, j));
-                            tc::st_async_v4(tc::sw128(peer_base + s * kBSlot + kBP, t, j), pv.x, pv.y, pv.z, pv.w, fb);
+                            tc::st_async_v4(tc::sw128(centry + kCP, t, j), pv.x, pv.y, pv.z, pv.w, fb);
                         }
+                        float v[64];
+                        t_row(gt + kGbb, v);
+                        const uint32_t t2 = peer_base + kARing + a * kAEntry + kAT2;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            tc::st_async_v4(tc::sw128(t2, t, j), tc::pack_bf16(v[8 * j], v[8 * j + 1]),
+                                            tc::pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                                            tc::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                                            tc::pack_bf16(v[8 * j + 6], v[8 * j + 7]), fb);
                     }
-                    const float* cs = gt + (row < 64 ? kGbeg : kGbb);
-                    const uint32_t tp = peer_base + kBTP + (row < 64 ? 0u : 16384u);
+                    if (GDN) {  // -w row i = row, as [i][t]
+                        wait(bar(F_WD + grp), uf & 1);
+                        __syncwarp();
+                        tc::tc_fence_after();
 #pragma unroll
-                    for (int jb = 0; jb < 4; ++jb) {
-                        float v16[16];
-                        if (GDN && jb <= (t >> 4)) {
-                            const float* Tr = tri_block_row(AF, t, jb);
+                        for (int half = 0; half < 2; ++half) {
+                            float x[32];
+                            tc::tmem_ld32(tmem + lane_off + kFColW + 64 * grp + 32 * half, x);
+                            tc::tmem_wait_ld();
 #pragma unroll
-                            for (int e = 0; e < 16; e += 4) {
-                                const float4 tv = *reinterpret_cast<const float4*>(Tr + e);
-                                const float4 sv = *reinterpret_cast<const float4*>(cs + 16 * jb + e);
-                                v16[e] = tv.x * sv.x; v16[e + 1] = tv.y * sv.y;
-                                v16[e + 2] = tv.z * sv.z; v16[e + 3] = tv.w * sv.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) v16[e] = (!GDN && 16 * jb + e == t) ? cs[t] : 0.f;
+                            for (int j = 0; j < 4; ++j)
+                                tc::st_async_v4(tc::sw128(centry + kCW, row, 4 * half + j),
+                                                tc::pack_bf16(-x[8 * j], -x[8 * j + 1]),
+                                                tc::pack_bf16(-x[8 * j + 2], -x[8 * j + 3]),
+                                                tc::pack_bf16(-x[8 * j + 4], -x[8 * j + 5]),
+                                                tc::pack_bf16(-x[8 * j + 6], -x[8 * j + 7]), fb);
                         }
-#pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2)
-                            tc::st_async_v4(tc::sw128(tp, t, 2 * jb + h2), tc::pack_bf16(v16[8 * h2], v16[8 * h2 + 1]),
-                                            tc::pack_bf16(v16[8 * h2 + 2], v16[8 * h2 + 3]),
-                                            tc::pack_bf16(v16[8 * h2 + 4], v16[8 * h2 + 5]),
-                                            tc::pack_bf16(v16[8 * h2 + 6], v16[8 * h2 + 7]), fb);
                     }
                 }
-                tc::named_bar(nb, 128);  // AF, the P staging and the stage's gate values are free
+                tc::tc_fence_before();
+                tc::named_bar(nb, 128);  // AF, the stagings, DW and the stage are free
                 if (gissuer) {
                     tc::mbar_arrive(bar(F_PUSHED + grp));
                     tc::mbar_arrive(bar(F_EMPTY + grp));
                 }
+                __syncwarp();
             }
-            if (gissuer) tc::mbar_arrive(bar(F_FIN));
+            if (gissuer) tc::mma_commit(bar(F_FIN));  // once its last w MMA is done
+            __syncwarp();
         }
     } else {
         // ============================================================ BACK
         if (warp == 0) {
-            // ---- TMA, gates, slot arming
+            // ---- TMA into both rings, arming of the push, gates
             int issued = 0;
             for (int c = 0; c < nch && !dead; ++c) {
-                const int s = c & 1, u = c >> 1;
-                const uint32_t st = sbase + s * kBSlot;
-                if (c >= 2) wait(bar(B_SLOTFREE + s), (u - 1) & 1);
+                const int e = c % 3, a = c & 1;
+                const uint32_t ce = sbase + e * kCEntry, ae = sbase + kARing + a * kAEntry;
+                if (c >= 3) wait(bar(B_CFREE + e), (c / 3 - 1) & 1);
+                if (c >= 2) wait(bar(B_AFREE + a), ((c >> 1) - 1) & 1);
                 const int t0 = start + c * kChunk;
                 if (lane == 0 && !*abort_flag) {
-                    tc::mbar_arrive_expect_tx(bar(B_FULLT + s), 3 * 16384 + (GDN ? 2048 : 0));
-                    tc::tma_load_3d(st + kBK0, &tm_k, 0, head, t0, bar(B_FULLT + s));
-                    tc::tma_load_3d(st + kBK1, &tm_k, 64, head, t0, bar(B_FULLT + s));
-                    tc::tma_load_3d(st + kBV0, &tm_v, 0, head, t0, bar(B_FULLT + s));
-                    tc::tma_load_3d(st + kBV1, &tm_v, 64, head, t0, bar(B_FULLT + s));
-                    tc::tma_load_3d(st + kBQ0, &tm_q, 0, head, t0, bar(B_FULLT + s));
-                    tc::tma_load_3d(st + kBQ1, &tm_q, 64, head, t0, bar(B_FULLT + s));
-                    if (GDN) {
-                        tc::tma_load_2d(st + kBGRaw, &tm_la, head & ~3, t0, bar(B_FULLT + s));
-                        tc::tma_load_2d(st + kBGRaw + 1024, &tm_b, head & ~3, t0, bar(B_FULLT + s));
-                    }
+                    tc::mbar_arrive_expect_tx(bar(B_FULLC + e), 4 * 8192);
+                    tc::tma_load_3d(ce + kCQ, &tm_q, 0, head, t0, bar(B_FULLC + e));
+                    tc::tma_load_3d(ce + kCQ + kBBox, &tm_q, 64, head, t0, bar(B_FULLC + e));
+                    tc::tma_load_3d(ce + kCK, &tm_k, 0, head, t0, bar(B_FULLC + e));
+                    tc::tma_load_3d(ce + kCK + kBBox, &tm_k, 64, head, t0, bar(B_FULLC + e));
+                    tc::mbar_arrive_expect_tx(bar(B_FULLA + a), 2 * 8192 + (GDN ? 1024 : 0));
+                    tc::tma_load_3d(ae + kAV, &tm_v, 0, head, t0, bar(B_FULLA + a));
+                    tc::tma_load_3d(ae + kAV + kBBox, &tm_v, 64, head, t0, bar(B_FULLA + a));
+                    if (GDN) tc::tma_load_2d(ae + kALa, &tm_la, head & ~3, t0, bar(B_FULLA + a));
                     issued = c + 1;
-                    // arm the push barrier of this slot, then tell the front
-                    tc::mbar_arrive_expect_tx(bar(B_FULLP + s), 8192 + 16384);
-                    tc::mbar_arrive_remote(peer_bar_f + 8u * (F_ARMED + s));
+                    // arm the push of the first three chunks (bytes counted on the chain
+                    // entry) and tell the front; the output warps arm the later ones
+                    if (c < 3) {
+                        tc::mbar_arrive_expect_tx(bar(B_FULLP + e), GDN ? 4 * 8192 : 2 * 8192);
+                        tc::mbar_arrive_remote(peer_bar_f + 8u * (F_ARMED + e));
+                    }
                     if (c + 2 < nch) {
                         const int tp = t0 + 2 * kChunk;
                         tc::tma_prefetch_3d(&tm_v, 0, head, tp);
@@ -544,190 +587,289 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     }
                 }
                 __syncwarp();
-                wait(bar(B_FULLT + s), u & 1);
-                const float* la_raw = reinterpret_cast<const float*>(sptr + s * kBSlot + kBGRaw);
-                derive_gates<GDN>(la_raw, la_raw + 256, head & 3, min(kChunk, len - c * kChunk),
-                                  reinterpret_cast<float*>(sptr + s * kBSlot + kBGate), lane);
-                if (lane == 0) tc::mbar_arrive(bar(B_GREADY + s));
+                wait(bar(B_FULLA + a), (c >> 1) & 1);
+                const float* la_raw = reinterpret_cast<const float*>(sptr + kARing + a * kAEntry + kALa);
+                derive_gates<GDN>(la_raw, la_raw, head & 3, min(kChunk, len - c * kChunk),
+                                  reinterpret_cast<float*>(sptr + e * kCEntry + kCGate), lane);
+                if (lane == 0) tc::mbar_arrive(bar(B_GREADY + e));
+                __syncwarp();
             }
             if (lane == 0 && *abort_flag)
-                for (int c = max(0, issued - 2); c < issued; ++c) tc::mbar_wait(bar(B_FULLT + (c & 1)), (c >> 1) & 1);
+                for (int c = max(0, issued - 2); c < issued; ++c) {
+                    tc::mbar_wait(bar(B_FULLC + c % 3), (c / 3) & 1);
+                    tc::mbar_wait(bar(B_FULLA + (c & 1)), (c >> 1) & 1);
+                }
+            __syncwarp();
         } else if (warp <= 4) {
-            // ---- apply: w = T' k (-> -w bf16), u = T'' v (-> the chain's D1), q~, k~
-            const bool aissuer = (warp == 4 && lane == 0);
+            // ---- output: o = e^g D1o (or D1o), thread = TMEM lane j (an o column)
+            const int j = row;
+            const bool ostore = (warp == 1 && lane == 0);
             for (int c = 0; c < nch && !dead; ++c) {
-                const int s = c & 1, u = c >> 1, b = c & 1;
-                const uint32_t st = sbase + s * kBSlot;
-                wait(bar(B_FULLT + s), u & 1);
-                wait.remote(bar(B_FULLP + s), u & 1);
-                if (aissuer) {
-                    if (c >= 2) wait(bar(B_D1F + b), ((c >> 1) - 1) & 1);
-                    if (!*abort_flag) {
-                        tc::tc_fence_after();
-                        if (GDN) {
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                tc::mma_bf16(tmem + kBColW, tc::sdesc(sbase + kBTP + kk * 32, 16, 1024),
-                                             tc::sdesc(st + kBK0 + kk * 2048, kBBlk, 1024), kIdP2w, kk > 0);
-                        }
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)  // D1 = [0; u]
-                            tc::mma_bf16(tmem + kBColD1 + b * 128, tc::sdesc(sbase + kBTP + 8192 + kk * 32, 16, 1024),
-                                         tc::sdesc(st + kBV0 + kk * 2048, 8192, 1024), kIdP2u, kk > 0);
-                        tc::mma_commit(bar(B_P2D));
-                    }
-                }
-                wait(bar(B_P2D), c & 1);
+                const int e = c % 3, b = c & 1;
+                const uint32_t ce = sbase + e * kCEntry;
+                const float* gt = reinterpret_cast<const float*>(sptr + e * kCEntry + kCGate);
+                wait(bar(B_M3 + b), (c >> 1) & 1);
+                wait(bar(B_GREADY + e), (c / 3) & 1);
+                __syncwarp();  // lanes may leave the waits apart; tcgen05.ld is warp-collective
                 tc::tc_fence_after();
-                if (aissuer) tc::mbar_arrive_remote(peer_bar_f + 8u * F_TPF);  // TP buffer consumed
-                wait(bar(B_GREADY + s), u & 1);
-                const float* gt = reinterpret_cast<const float*>(sptr + s * kBSlot + kBGate);
-                if (row < 64) {
-                    if (GDN) {  // -w row -> bf16 into the w boxes
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            float x[64];
-                            tc::tmem_ld32(tmem + lane_off + kBColW + 64 * half, *reinterpret_cast<float(*)[32]>(x));
-                            tc::tmem_ld32(tmem + lane_off + kBColW + 64 * half + 32,
-                                          *reinterpret_cast<float(*)[32]>(x + 32));
-                            tc::tmem_wait_ld();
-                            store_row64_neg(st + (half ? kBW1 : kBW0), row, x);
-                        }
-                    } else {
-                        scale_row(st + kBK0, row, gt[kGkdec + row]);
-                    }
-                } else {
-                    const int t = row - 64;
-                    if (GDN) {
-                        scale_row(st + kBQ0, t, gt[kGeg + t]);
-                        scale_row(st + kBK0, t, gt[kGkdec + t]);
-                    }
-                }
-                tc::fence_proxy_async();
+                float x[64];
+                tc::tmem_ld32(tmem + lane_off + kTD1o + 64 * b, *reinterpret_cast<float(*)[32]>(x));
+                tc::tmem_ld32(tmem + lane_off + kTD1o + 64 * b + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+                tc::tmem_wait_ld();
                 tc::tc_fence_before();
                 tc::named_bar(1, 128);
-                if (aissuer) tc::mbar_arrive(bar(B_READY + s));
-            }
-            if (aissuer) tc::mma_commit(bar(B_FIN));
-        } else {
-            // ---- the chain: 8 warps; thread = (row r of h, 64-column half hw)
-            const int hw = (warp - 5) >> 2;  // 0, 1
-            const int j0 = 64 * hw;
-            const int r = row;
-            const bool cissuer = (warp == 6 && lane == 0);  // row 64 of half 0
-            const size_t hoff = (((size_t)seq * H + head) * kD + r) * kD + j0;
-            const uint32_t hb = sbase + kBHB, vn = sbase + kBVN;
-            float h[64];
-            if (h0 && !dead) {
-#pragma unroll
-                for (int e = 0; e < 64; e += 4) {
-                    float4 v4 = *reinterpret_cast<const float4*>(h0 + hoff + e);
-                    h[e] = v4.x; h[e + 1] = v4.y; h[e + 2] = v4.z; h[e + 3] = v4.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 64; ++e) h[e] = 0.f;
-            }
-            store_row64(hb + hw * 16384, r, h);
-            tc::fence_proxy_async();
-            tc::named_bar(2, 256);
-            for (int c = 0; c < nch && !dead; ++c) {
-                const int s = c & 1, u = c >> 1, b = c & 1;
-                const uint32_t st = sbase + s * kBSlot;
-                const uint32_t d1 = tmem + kBColD1 + b * 128;
-                wait(bar(B_READY + s), u & 1);
-                const float* gt = reinterpret_cast<const float*>(sptr + s * kBSlot + kBGate);
-                if (cissuer && !*abort_flag) {  // D1 = [0; u] + [q~; -w] h
-                    tc::tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_bf16(d1, tc::sdesc(st + kBQ0 + (kk >> 2) * kBBlk + (kk & 3) * 32, 16, 1024),
-                                     tc::sdesc(hb + kk * 2048, 16384, 1024), kId1, 1);
-                    tc::mma_commit(bar(B_M1));
-                }
-                if (r >= 64) {  // rows 64..127 of D1 now hold v_new
-                    wait(bar(B_M1), c & 1);
-                    tc::tc_fence_after();
-                    const int t = r - 64;
-#pragma unroll
-                    for (int part = 0; part < 4; ++part) {
-                        float x[16];
-                        tc::tmem_ld16(d1 + lane_off + j0 + 16 * part, x);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int q8 = 0; q8 < 2; ++q8)
-                            tc::st_shared_v4(tc::sw128(vn + hw * 8192, t, 2 * part + q8),
-                                             tc::pack_bf16(x[8 * q8], x[8 * q8 + 1]),
-                                             tc::pack_bf16(x[8 * q8 + 2], x[8 * q8 + 3]),
-                                             tc::pack_bf16(x[8 * q8 + 4], x[8 * q8 + 5]),
-                                             tc::pack_bf16(x[8 * q8 + 6], x[8 * q8 + 7]));
-                    }
-                    tc::fence_proxy_async();
-                    tc::tc_fence_before();
-                    tc::named_bar(3, 128);
-                    if (cissuer && !*abort_flag) {
-                        tc::tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)  // D2 = k~^T v_new
-                            tc::mma_bf16(tmem + kBColD2, tc::sdesc(st + kBK0 + kk * 2048, kBBlk, 1024),
-                                         tc::sdesc(vn + kk * 2048, 8192, 1024), kId2, kk > 0);
-                        tc::mma_commit(bar(B_M2));
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)  // D1[0:64] += P v_new
-                            tc::mma_bf16(d1, tc::sdesc(st + kBP + kk * 32, 16, 1024),
-                                         tc::sdesc(vn + kk * 2048, 8192, 1024), kId3, 1);
-                        tc::mma_commit(bar(B_M3));
+                if (ostore) {
+                    tc::mbar_arrive(bar(B_D1OF + b));
+                    // chunk c's MMAs are done with -w and P^ of this chain entry: arm the
+                    // push of chunk c + 3 once u of chunk c + 1 has also freed its T''
+                    if (c + 3 < nch) {
+                        wait(bar(B_AFREE + ((c + 1) & 1)), ((c + 1) >> 1) & 1);
+                        tc::mbar_arrive_expect_tx(bar(B_FULLP + e), GDN ? 4 * 8192 : 2 * 8192);
+                        tc::mbar_arrive_remote(peer_bar_f + 8u * (F_ARMED + e));
                     }
                 }
-                wait(bar(B_M2), c & 1);
-                tc::tc_fence_after();
-                {
-                    const float egl = gt[kGscal + 0];
+                __syncwarp();  // lane 0 may have waited above
+                const bool fold = gt[kGscal + 1] != 0.f;
+                const int n = min(kChunk, len - c * kChunk);
+                const int t0 = start + c * kChunk;
+                if (n == kChunk) {
+                    // stage o as two [64 t][64 j] SW128 boxes in the k tile (k is dead
+                    // once D1o is complete), then one TMA store per box.  Row t = 8u + r
+                    // of the swizzled box sits at u * 1024 + off[r].
+                    const uint32_t box = ce + kCK + (uint32_t)(j >> 6) * kBBox;
+                    const uint32_t ch = (uint32_t)(j & 63) >> 3, jj = (uint32_t)(j & 7) * 2;
+                    uint32_t off[8];
 #pragma unroll
-                    for (int part = 0; part < 4; ++part) {
-                        float dd[16];
-                        tc::tmem_ld16(tmem + kBColD2 + lane_off + j0 + 16 * part, dd);
-                        tc::tmem_wait_ld();
+                    for (int r = 0; r < 8; ++r) off[r] = box + r * 128 + ((ch ^ r) << 4) + jj;
+                    if (fold) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) h[16 * part + e] = fmaf(egl, h[16 * part + e], dd[e]);
-                    }
-                }
-                if (c + 1 < nch) store_row64(hb + hw * 16384, r, h);
-                tc::fence_proxy_async();
-                tc::tc_fence_before();
-                tc::named_bar(2, 256);
-                if (r < 64) {  // o = rows 0..63 of D1
-                    wait(bar(B_M3), c & 1);
-                    tc::tc_fence_after();
-                    if (r == 0 && hw == 0) tc::mbar_arrive(bar(B_SLOTFREE + s));
-                    const int n = min(kChunk, len - c * kChunk);
-                    const int t0 = start + c * kChunk;
-#pragma unroll
-                    for (int part = 0; part < 4; ++part) {
-                        float oo[16];
-                        tc::tmem_ld16(d1 + lane_off + j0 + 16 * part, oo);
-                        tc::tmem_wait_ld();
-                        if (r < n && !*abort_flag) {
-                            uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(t0 + r) * H + head) * kD + j0 + 16 * part);
-#pragma unroll
-                            for (int q8 = 0; q8 < 2; ++q8)
-                                dst[q8] = make_uint4(tc::pack_bf16(oo[8 * q8], oo[8 * q8 + 1]),
-                                                     tc::pack_bf16(oo[8 * q8 + 2], oo[8 * q8 + 3]),
-                                                     tc::pack_bf16(oo[8 * q8 + 4], oo[8 * q8 + 5]),
-                                                     tc::pack_bf16(oo[8 * q8 + 6], oo[8 * q8 + 7]));
+                        for (int t4 = 0; t4 < 16; ++t4) {
+                            const float4 eg = *reinterpret_cast<const float4*>(gt + kGeg + 4 * t4);
+                            x[4 * t4] *= eg.x;
+                            x[4 * t4 + 1] *= eg.y;
+                            x[4 * t4 + 2] *= eg.z;
+                            x[4 * t4 + 3] *= eg.w;
                         }
                     }
-                    tc::tc_fence_before();
+#pragma unroll
+                    for (int t = 0; t < 64; ++t)
+                        st_shared_u16(off[t & 7] + (t >> 3) * 1024, __bfloat16_as_ushort(__float2bfloat16_rn(x[t])));
+                    tc::fence_proxy_async();
+                    tc::named_bar(1, 128);
+                    if (ostore) {
+                        if (!*abort_flag) {
+                            tc::tma_store_3d(&tm_o, ce + kCK, 0, head, t0);
+                            tc::tma_store_3d(&tm_o, ce + kCK + kBBox, 64, head, t0);
+                            tc::bulk_commit();
+                        }
+                        tc::bulk_wait_read0();
+                        tc::mbar_arrive(bar(B_CFREE + e));
+                    }
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(bar(B_D1F + b));
+                } else {
+                    // the sequence's last, partial chunk: plain stores of the valid rows
+                    if (!*abort_flag) {
+#pragma unroll
+                        for (int t = 0; t < 64; ++t)
+                            if (t < n)
+                                o[((size_t)(t0 + t) * H + head) * kD + j] =
+                                    __float2bfloat16_rn(fold ? x[t] * gt[kGeg + t] : x[t]);
+                    }
+                    tc::named_bar(1, 128);
+                    if (ostore) tc::mbar_arrive(bar(B_CFREE + e));
+                    __syncwarp();
                 }
             }
-            if (h_T && !*abort_flag && !dead) {
+            if (ostore) tc::bulk_wait0();
+            __syncwarp();
+        } else if (warp <= 12) {
+            // ---- the state chain: 8 warps; thread = (state row j = TMEM lane, half hh).
+            // S = h^T (dv x dk) lives in TMEM: fp32 in D2 (the MMA accumulates the
+            // chunk update onto it) and bf16 in TS (the A operand of the MMAs with q
+            // and -w).
+            const int hh = (warp - 5) >> 2;
+            const int j = row;
+            const int ct = tid - 160;  // 0..255
+            const bool cl = (warp == 5 && lane == 0);  // signals the MMA warp
+            const size_t hbase = ((size_t)seq * H + head) * kD * kD;  // h[i][j] at hbase + i * kD + j
+            const uint32_t d2 = tmem + lane_off + kTD2 + 64 * hh;
+            const uint32_t ts = tmem + lane_off + kTS + 32 * hh;
+            // S (bf16) <- S (fp32)
+            auto snapshot = [&]() {
 #pragma unroll
-                for (int e = 0; e < 64; e += 4)
-                    *reinterpret_cast<float4*>(h_T + hoff + e) = make_float4(h[e], h[e + 1], h[e + 2], h[e + 3]);
+                for (int part = 0; part < 2; ++part) {
+                    float d[32];
+                    tc::tmem_ld32(d2 + 32 * part, d);
+                    tc::tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) pk[e2] = tc::pack_bf16(d[2 * e2], d[2 * e2 + 1]);
+                    tc::tmem_st16(ts + 16 * part, pk);
+                }
+                tc::tmem_wait_st();
+            };
+            // S (fp32) *= f
+            auto decay = [&](float f) {
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {
+                    float d[16];
+                    tc::tmem_ld16(d2 + 16 * part, d);
+                    tc::tmem_wait_ld();
+                    uint32_t r[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) r[e2] = __float_as_uint(d[e2] * f);
+                    tc::tmem_st16(d2 + 16 * part, r);
+                }
+                tc::tmem_wait_st();
+            };
+            // strong-decay chunk: q~ = e^g q and k~ = e^{g_last - g} k in place
+            auto prescale = [&](int c) {
+                const int e = c % 3;
+                wait(bar(B_FULLC + e), (c / 3) & 1);
+                wait(bar(B_GREADY + e), (c / 3) & 1);
+                __syncwarp();
+                const float* gt = reinterpret_cast<const float*>(sptr + e * kCEntry + kCGate);
+                if (gt[kGscal + 1] == 0.f) {
+                    const int which = ct >> 7, t = (ct >> 1) & 63, bx = ct & 1;
+                    const uint32_t rowbox = sbase + e * kCEntry + (which ? kCK : kCQ) + bx * kBBox;
+                    const float f = which ? gt[kGkdec + t] : gt[kGeg + t];
+                    const __nv_bfloat162 f2 = __float2bfloat162_rn(f);
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const uint32_t ad = tc::sw128(rowbox, t, jj);
+                        uint4 v4 = tc::ld_shared_v4(ad);
+                        __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&v4);
+                        p2[0] = __hmul2(p2[0], f2);
+                        p2[1] = __hmul2(p2[1], f2);
+                        p2[2] = __hmul2(p2[2], f2);
+                        p2[3] = __hmul2(p2[3], f2);
+                        tc::st_shared_v4(ad, v4.x, v4.y, v4.z, v4.w);
+                    }
+                    tc::fence_proxy_async();
+                }
+                return gt[kGscal + 0];  // e^{g_last} of chunk c
+            };
+            {  // S from h0 (h0[i][j], i = 64 hh + x)
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x)
+                        r[x] = __float_as_uint((h0 && !dead) ? h0[hbase + (size_t)(64 * hh + 16 * part + x) * kD + j] : 0.f);
+                    tc::tmem_st16(d2 + 16 * part, r);
+                }
+                tc::tmem_wait_st();
             }
-            if (cissuer) tc::mma_commit(bar(B_FIN));
+            snapshot();
+            if (nch > 0 && !dead) {
+                const float egl0 = prescale(0);
+                if (GDN) decay(egl0);
+            }
+            tc::tc_fence_before();
+            tc::named_bar(2, 256);
+            if (cl) tc::mbar_arrive(bar(B_SREADY));
+            __syncwarp();
+            for (int c = 0; c < nch && !dead; ++c) {
+                const int e = c % 3, b = c & 1;
+                const float* gt = reinterpret_cast<const float*>(sptr + e * kCEntry + kCGate);
+                // (1) v^ = e^{g_last - g} v_new (or v_new), bf16 into TMEM
+                wait(bar(B_GREADY + e), (c / 3) & 1);
+                wait(bar(B_M1W), c & 1);
+                __syncwarp();
+                tc::tc_fence_after();
+                const bool fold = gt[kGscal + 1] != 0.f;
+                {
+                    float x[32];
+                    tc::tmem_ld32(tmem + lane_off + kTD1v + 64 * b + 32 * hh, x);
+                    tc::tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const float2 kd = fold ? *reinterpret_cast<const float2*>(gt + kGkdec + 32 * hh + 2 * e2)
+                                               : make_float2(1.f, 1.f);
+                        pk[e2] = tc::pack_bf16(x[2 * e2] * kd.x, x[2 * e2 + 1] * kd.y);
+                    }
+                    tc::tmem_st16(tmem + lane_off + kTVN + 16 * hh, pk);
+                    tc::tmem_wait_st();
+                }
+                tc::tc_fence_before();
+                tc::named_bar(2, 256);
+                if (cl) tc::mbar_arrive(bar(B_VREADY));
+                __syncwarp();
+                // (2) S (bf16) for the next chunk's MMAs; q, k of a strong-decay next chunk
+                wait(bar(B_M2), c & 1);
+                __syncwarp();
+                tc::tc_fence_after();
+                float egl_next = 1.f;
+                if (c + 1 < nch) {
+                    snapshot();
+                    egl_next = prescale(c + 1);
+                }
+                tc::tc_fence_before();
+                tc::named_bar(2, 256);
+                if (cl && c + 1 < nch) tc::mbar_arrive(bar(B_SREADY));
+                __syncwarp();
+                // (3) while the next MMAs run: S (fp32) <- e^{g_last} S for the next chunk;
+                // the named barrier after the next v^ orders it before the next S += v^^T k
+                if (GDN && c + 1 < nch) decay(egl_next);
+            }
+            if (h_T && !*abort_flag && !dead) {
+                tc::tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {
+                    float d[16];
+                    tc::tmem_ld16(d2 + 16 * part, d);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) h_T[hbase + (size_t)(64 * hh + 16 * part + x) * kD + j] = d[x];
+                }
+            }
+        } else {
+            // ---- the MMA warp: every MMA of the back, in chunk order
+            const bool L = lane == 0;
+            for (int c = 0; c < nch && !dead; ++c) {
+                const int e = c % 3, a = c & 1, b = c & 1;
+                const uint32_t ce = sbase + e * kCEntry, ae = sbase + kARing + a * kAEntry;
+                // D1v[b] = u^T = v^T T''^T
+                wait(bar(B_FULLA + a), (c >> 1) & 1);
+                wait.remote(bar(B_FULLP + e), (c / 3) & 1);
+                if (!*abort_flag) {
+                    tc::tc_fence_after();
+                    tc::mma_batch_ss(L, tmem + kTD1v + 64 * b, tc::sdesc(ae + kAV, kBBox, 1024), 128,
+                                     tc::sdesc(ae + kAT2, 16, 1024), 2, kIdWU, 4, false);
+                    tc::mma_commit_p(L, bar(B_AFREE + a));
+                }
+                // D1v[b] += S (-w)^T once S(c) is in TMEM
+                wait(bar(B_SREADY), c & 1);
+                wait(bar(B_FULLC + e), (c / 3) & 1);
+                if (!*abort_flag) {
+                    tc::tc_fence_after();
+                    if (GDN)
+                        tc::mma_batch_ts(L, tmem + kTD1v + 64 * b, tmem + kTS, 8, tc::sdesc(ce + kCW, kBBox, 1024), 128,
+                                         kId1w, 8, true);
+                    tc::mma_commit_p(L, bar(B_M1W));
+                }
+                // D1o[b] = S q^T once the output warps have read D1o[b]
+                if (c >= 2) wait(bar(B_D1OF + b), ((c >> 1) - 1) & 1);
+                if (!*abort_flag) {
+                    tc::tc_fence_after();
+                    tc::mma_batch_ts(L, tmem + kTD1o + 64 * b, tmem + kTS, 8, tc::sdesc(ce + kCQ, 16, 1024), 2, kId1q, 4,
+                                     false);
+                    tc::mma_batch_ts(L, tmem + kTD1o + 64 * b, tmem + kTS + 32, 8, tc::sdesc(ce + kCQ + kBBox, 16, 1024), 2,
+                                     kId1q, 4, true);
+                }
+                // S += v^^T k; D1o[b] += v^^T P^^T
+                wait(bar(B_VREADY), c & 1);
+                if (!*abort_flag) {
+                    tc::tc_fence_after();
+                    tc::mma_batch_ts(L, tmem + kTD2, tmem + kTVN, 8, tc::sdesc(ce + kCK, kBBox, 1024), 128, kId2, 4, true);
+                    tc::mma_commit_p(L, bar(B_M2));
+                    tc::mma_batch_ts(L, tmem + kTD1o + 64 * b, tmem + kTVN, 8, tc::sdesc(ce + kCP, 16, 1024), 2, kId3, 4,
+                                     true);
+                    tc::mma_commit_p(L, bar(B_M3 + b));
+                }
+            }
+            tc::mma_commit_p(L, bar(B_FIN));
         }
     }
 
@@ -736,6 +878,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0) tc::mbar_wait(bar(front ? F_FIN : B_FIN), 0);
+    __syncwarp();
     __syncthreads();
     tc::tc_fence_after();
     if (warp == 0) tc::tmem_dealloc(tmem, front ? kFTmemCols : kBTmemCols);
@@ -759,11 +902,11 @@ cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t st) {
     const long long units = (long long)a.n_seqs * a.H;
     if (units == 0) return cudaSuccess;
     if (2 * units > 0x7fffffffLL) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv, mla, mb;
+    CUtensorMap mq, mk, mv, mla, mb, mo;
     const int64_t T = a.T_total > 0 ? a.T_total : 1;
     const void* base = a.q ? a.q : a.ws;
     if (!encode_token_map(&mq, a.q ? a.q : base, T, a.H) || !encode_token_map(&mk, a.k ? a.k : base, T, a.H) ||
-        !encode_token_map(&mv, a.v ? a.v : base, T, a.H))
+        !encode_token_map(&mv, a.v ? a.v : base, T, a.H) || !encode_token_map(&mo, a.o ? a.o : base, T, a.H))
         return cudaErrorInvalidValue;
     if (a.delta_rule) {
         if (!encode_gate_map(&mla, a.log_alpha ? a.log_alpha : (const float*)base, T, a.H) ||
@@ -788,7 +931,7 @@ cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mla, mb, a.h0, (__nv_bfloat16*)a.o, a.h_T, a.ws, a.H);
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mla, mb, mo, a.h0, (__nv_bfloat16*)a.o, a.h_T, a.ws, a.H);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

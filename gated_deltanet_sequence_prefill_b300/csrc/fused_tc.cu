@@ -182,7 +182,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
     if (hdr->status != GDN_OK) return;
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the warp index and the TMEM base are broadcast from lane 0 so that the
+    // compiler sees them as warp-uniform: role branches then stay in uniform
+    // control flow and MMA descriptors are built in uniform registers
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
     const int n_seqs = hdr->n_seqs;
     PlanLayout L(n_seqs);
     const int* cu = reinterpret_cast<const int*>(ws + L.cu);
@@ -191,7 +195,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int seq = order[unit / (2 * H)];
     const int rem = unit % (2 * H);
     const int head = rem >> 1, j0 = (rem & 1) * kNv;
-    const int start = cu[seq], len = cu[seq + 1] - start;
+    // loaded values, broadcast so that loops over chunks count as warp-uniform
+    const int start = __shfl_sync(0xffffffffu, cu[seq], 0);
+    const int len = __shfl_sync(0xffffffffu, cu[seq + 1], 0) - start;
     const int nch = (len + kChunk - 1) / kChunk;
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + kOffMisc);
@@ -217,11 +223,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         tc::fence_proxy_async();
     }
+    __syncwarp();  // lane-0-only work above: reconverge before any .aligned instruction
     if (warp == 0) tc::tmem_alloc(sbase + kOffMisc + 8, kTmemCols);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
     const int quad = warp & 3;                        // TMEM lane quadrant of this warp
     const int row = 32 * quad + lane;                 // TMEM lane / tile row
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
@@ -284,6 +291,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (c >= 2) wait(bar(B_P1F + (c & 1)), ((c >> 1) - 1) & 1);
                 if (!*abort_flag) issue_p1(c);
             }
+            __syncwarp();
             // derived gate values of the chunk
             const int n = min(kChunk, len - c * kChunk);
             float* gt = gate(s);
@@ -333,11 +341,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(B_GREADY + s));
+            __syncwarp();
         }
         // after an abort, let copies already issued land before the CTA exits
         if (lane == 0 && *abort_flag)
             for (int c = max(0, issued - 2); c < issued; ++c)
                 tc::mbar_wait(bar(B_FULL + (c & 1)), (c >> 1) & 1);
+        __syncwarp();
     } else if (warp <= 4) {
         // ================================================== solve group
         const int pw = warp - 1;  // 0..3
@@ -348,6 +358,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t st = sbase + s * kStage;
             wait(bar(B_GREADY + s), u & 1);
             wait(bar(B_P1D + (c & 1)), u & 1);
+            __syncwarp();
             tc::tc_fence_after();
             const float* gt = gate(s);
             const bool safe = gt[kGscal + 1] != 0.f;
@@ -360,6 +371,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc::tc_fence_before();
             tc::named_bar(1, 128);  // DP1[c & 1] fully read
             if (solve_issuer) tc::mbar_arrive(bar(B_P1F + (c & 1)));
+            __syncwarp();
             // rows 0..63: K K^T -> A (fp32); rows 64..127: Q K^T -> P (bf16 tile)
             {
                 const int t = row & 63;
@@ -432,6 +444,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc::fence_proxy_async();
             tc::named_bar(1, 128);
             if (solve_issuer) tc::mbar_arrive(bar(B_TPR + (c & 1)));
+            __syncwarp();
         }
     } else if (warp <= 8) {
         // ================================================== apply group
@@ -456,9 +469,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                  tc::sdesc(st + kOffV + kk * 2048, 8192, 1024), kIdP2u, kk > 0);
                 tc::mma_commit(bar(B_P2D));
             }
+            __syncwarp();
             wait(bar(B_P2D), c & 1);
+            __syncwarp();
             tc::tc_fence_after();
             if (apply_issuer) tc::mbar_arrive(bar(B_TPF + (c & 1)));
+            __syncwarp();
             const float* gt = gate(s);
             if (row < 64) {
                 if (GDN) {  // w row -> bf16 into the w boxes
@@ -487,6 +503,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc::tc_fence_before();
             tc::named_bar(2, 128);
             if (apply_issuer) tc::mbar_arrive(bar(B_READY + s));
+            __syncwarp();
         }
     } else {
         // ================================================== state chain
@@ -522,9 +539,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                  tc::sdesc(sbase + kOffHB + kk * 2048, 8192, 1024), kId1, kk > 0);
                 tc::mma_commit(bar(B_M1));
             }
+            __syncwarp();
             if (r >= 64) {
                 // ---- v_new = u - w h   (rows 64..127 of D1 are w h)
                 wait(bar(B_M1), c & 1);
+                __syncwarp();
                 tc::tc_fence_after();
                 const int t = r - 64;
 #pragma unroll
@@ -565,9 +584,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tc::mma_commit(bar(B_M3));
                     }
                 }
+                __syncwarp();
             }
             // ---- h <- e^{g_last} h + k~^T v_new
             wait(bar(B_M2), c & 1);
+            __syncwarp();
             tc::tc_fence_after();
             {
                 const float egl = gt[kGscal + 0];
@@ -587,8 +608,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // ---- o = rows 0..63 of D1
             if (r < 64) {
                 wait(bar(B_M3), c & 1);
+                __syncwarp();
                 tc::tc_fence_after();
                 if (r == 0) tc::mbar_arrive(bar(B_EMPTY + s));  // every MMA reading the stage has retired
+                __syncwarp();
                 const int n = min(kChunk, len - c * kChunk);
                 const int t0 = start + c * kChunk;
 #pragma unroll
@@ -619,9 +642,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // drain: every MMA issuer commits once more; wait (bounded) until every
     // MMA of this CTA has completed before the tensor memory is released
     if (tma_issuer || solve_issuer || apply_issuer || state_issuer) tc::mma_commit(bar(B_FIN));
+    __syncwarp();
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0) tc::mbar_wait(bar(B_FIN), 0);
+    __syncwarp();
     __syncthreads();
     tc::tc_fence_after();
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);

@@ -81,6 +81,7 @@ plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs, long long T_total, ch
     if (tid == 0) {
         hdr->status = GDN_OK;
         hdr->counter = 0;
+        hdr->pad[0] = 0;
         hdr->n_seqs = n_seqs;
         hdr->total_chunks = s_carry;
         hdr->max_len = s_maxlen;

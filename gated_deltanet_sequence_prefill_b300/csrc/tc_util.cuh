@@ -87,6 +87,19 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
                  "r"(x), "r"(y)
                  : "memory");
 }
+// Store a box from shared memory to global (bulk-group completion).  The
+// caller keeps x 16-byte aligned and never starts at a negative coordinate.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the committed stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until the committed stores are complete.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -134,6 +147,58 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// The same MMA with the A operand read from tensor memory: lane = row of A,
+// two bf16 per 32-bit column (even k in the low half), 8 columns per K = 16.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0;"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Warp-converged forms: every lane of the warp executes the instruction and
+// only `leader` issues it (a lone diverged issuer pays far more per MMA).
+__device__ __forceinline__ void mma_bf16_p(bool leader, uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p, l; setp.ne.b32 p, %4, 0; setp.ne.b32 l, %5, 0;"
+        " @l tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"((uint32_t)leader)
+        : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ta_p(bool leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p, l; setp.ne.b32 p, %4, 0; setp.ne.b32 l, %5, 0;"
+        " @l tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"((uint32_t)leader)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_p(bool leader, uint32_t bar) {
+    asm volatile(
+        "{ .reg .pred l; setp.ne.b32 l, %1, 0;"
+        " @l tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }" ::"r"(bar),
+        "r"((uint32_t)leader)
+        : "memory");
+}
+// n K-slices of one MMA shape from a single issue site (warp-converged,
+// `leader` issues).  Descriptors advance by a_step / b_step 16-byte units per
+// slice (a TMEM A operand by a_step columns).  Keeping every MMA of a loop on
+// these two sites keeps the issue cost near the tensor pipe's own rate; many
+// distinct inline MMA sites in one loop issue several times slower.
+static __device__ __noinline__ void mma_batch_ss(bool leader, uint32_t d, uint64_t a0, uint32_t a_step, uint64_t b0,
+                                          uint32_t b_step, uint32_t idesc, int n, bool acc0) {
+#pragma unroll 1
+    for (int k = 0; k < n; ++k)
+        mma_bf16_p(leader, d, a0 + (uint64_t)(k * a_step), b0 + (uint64_t)(k * b_step), idesc, (k > 0) || acc0);
+}
+static __device__ __noinline__ void mma_batch_ts(bool leader, uint32_t d, uint32_t a0, uint32_t a_step, uint64_t b0,
+                                          uint32_t b_step, uint32_t idesc, int n, bool acc0) {
+#pragma unroll 1
+    for (int k = 0; k < n; ++k)
+        mma_bf16_ta_p(leader, d, a0 + k * a_step, b0 + (uint64_t)(k * b_step), idesc, (k > 0) || acc0);
+}
 // Arrive on `bar` once every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -170,6 +235,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Store 16 / 32 consecutive 32-bit columns of this warp's 32 lanes (lane = row).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -214,6 +291,26 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     uint32_t ok;
     asm volatile(
         "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;"
+        " selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Non-blocking probes of the same phases.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;"
         " selp.u32 %0, 1, 0, p; }"
         : "=r"(ok)
         : "r"(bar), "r"(parity)

@@ -93,6 +93,35 @@ def test_gdn_ragged_varlen(g, dk, dv, dtype, staged):
     assert rel(hT, rh) <= TOL[dtype], rel(hT, rh)
 
 
+@pytest.mark.parametrize("scale", [6.0, 40.0])
+def test_gdn_strong_gates(g, scale):
+    """Strongly negative log-decays: a chunk's decay range (about 30 at scale
+    6, about 200 at scale 40) straddles or passes the limit of the factored
+    form, so both decay paths of the fused kernel run."""
+    inp = gi.gdn_inputs([700, 333, 129], 4, 128, 128, "bf16", h0_std=0.5, seed=5)
+    inp["log_alpha"] = inp["log_alpha"] * scale
+    o, hT = run_gdn(g, inp)
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
+    assert rel(hT, rh) <= TOL["bf16"], rel(hT, rh)
+
+
+@pytest.mark.parametrize("lengths,h0_std,strong", [([1, 70, 0, 129, 64, 200, 63], 0.01, False),
+                                                   ([700, 333], 0.5, True)])
+def test_single_sm_kernel(g, monkeypatch, lengths, h0_std, strong):
+    """The single-SM fused kernel (selected through the environment) against
+    the oracle: ragged sequences, and strong gates that take its unfactored
+    decay path."""
+    monkeypatch.setenv("GDN_PREFILL_SINGLE_SM", "1")
+    inp = gi.gdn_inputs(lengths, 4, 128, 128, "bf16", h0_std=h0_std, seed=3)
+    if strong:
+        inp["log_alpha"] = inp["log_alpha"] * 40.0
+    o, hT = run_gdn(g, inp)
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
+    assert rel(hT, rh) <= TOL["bf16"], rel(hT, rh)
+
+
 @pytest.mark.parametrize("seed", [1, 2])
 def test_gdn_seeds(g, seed):
     inp = gi.gdn_inputs([300, 777], 4, 128, 128, "bf16", h0_std=0.01, seed=seed)
