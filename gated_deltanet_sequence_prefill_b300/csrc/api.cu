@@ -76,16 +76,17 @@ PrefillArgs make_args(const void* q, const void* k, const void* v, const float* 
     return a;
 }
 
-// The 2-SM cluster kernel (solve and state pass on separate SMs) is the
-// default; GDN_PREFILL_SINGLE_SM=1 in the environment selects the single-SM
-// kernel (one CTA per sequence, head and 64-column half of the state).
-bool single_sm_requested() {
-    const char* e = getenv("GDN_PREFILL_SINGLE_SM");
+// The single-SM fused kernel (one CTA per sequence, head and 64-column half
+// of the state) is the default; GDN_PREFILL_PAIR=1 in the environment selects
+// the 2-SM cluster kernel (solve and state pass on separate SMs), which is
+// faster when few (sequence, head) units share the GPU.
+bool pair_requested() {
+    const char* e = getenv("GDN_PREFILL_PAIR");
     return e != nullptr && e[0] == '1';
 }
 
 gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
-    const bool pair = !single_sm_requested() && pair_supported(a);
+    const bool pair = pair_requested() && pair_supported(a);
     const bool fused = pair || fused_supported(a);
     size_t need = plan_bytes(a.n_seqs);
     if (!fused) need += staged_intermediate_bytes(a.T_total, a.H, a.dk, a.dv, a.n_seqs);

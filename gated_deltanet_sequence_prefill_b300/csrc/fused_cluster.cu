@@ -161,23 +161,26 @@ __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_fla
 }
 
 // Bounded waits that stop waiting once this CTA has aborted; every thread
-// keeps executing the same sequence of named barriers after an abort.
+// keeps executing the same sequence of named barriers after an abort.  The
+// wait is one out-of-line function: inlined at every call site its loop and
+// timeout path made up a large share of the kernel's instruction footprint.
+static __device__ __noinline__ bool wait_bar(volatile int* abort_flag, char* ws, uint32_t bar, uint32_t parity,
+                                             int site, bool cluster_scope) {
+    if (*abort_flag) return false;
+    if (cluster_scope ? tc::mbar_wait_cluster(bar, parity) : tc::mbar_wait(bar, parity)) return true;
+    report_timeout(ws, abort_flag, site);
+    return false;
+}
 struct Waiter {
     volatile int* abort_flag;
     char* ws;
     uint32_t bar_base;
     int site_base;
     __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
-        if (*abort_flag) return false;
-        if (tc::mbar_wait(bar, parity)) return true;
-        report_timeout(ws, abort_flag, site_base + (int)((bar - bar_base) >> 3));
-        return false;
+        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), false);
     }
     __device__ __forceinline__ bool remote(uint32_t bar, uint32_t parity) const {
-        if (*abort_flag) return false;
-        if (tc::mbar_wait_cluster(bar, parity)) return true;
-        report_timeout(ws, abort_flag, site_base + (int)((bar - bar_base) >> 3));
-        return false;
+        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), true);
     }
 };
 
@@ -206,7 +209,7 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
 // (rows past the chunk end contribute nothing), exp(g), exp(-g), beta,
 // beta e^g, k decay exp(g_last - g) (0 past the end), and the scalars.
 template <bool GDN>
-__device__ __forceinline__ void derive_gates(const float* la_raw, const float* b_raw, int hc, int n,
+__device__ __noinline__ void derive_gates(const float* la_raw, const float* b_raw, int hc, int n,
                                              float* gt, int lane) {
     const int ta = lane, tb = lane + 32;
     float ga = 0.f, gb = 0.f, ba, bb;
@@ -669,11 +672,15 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 } else {
                     // the sequence's last, partial chunk: plain stores of the valid rows
                     if (!*abort_flag) {
+                        // (x is consumed through shared memory so that this rarely
+                        // taken path stays a short loop)
+                        float* xs = reinterpret_cast<float*>(sptr + e * kCEntry + kCK) + j * 65;
 #pragma unroll
-                        for (int t = 0; t < 64; ++t)
-                            if (t < n)
-                                o[((size_t)(t0 + t) * H + head) * kD + j] =
-                                    __float2bfloat16_rn(fold ? x[t] * gt[kGeg + t] : x[t]);
+                        for (int t = 0; t < 64; ++t) xs[t] = x[t];
+#pragma unroll 1
+                        for (int t = 0; t < n; ++t)
+                            o[((size_t)(t0 + t) * H + head) * kD + j] =
+                                __float2bfloat16_rn(fold ? xs[t] * gt[kGeg + t] : xs[t]);
                     }
                     tc::named_bar(1, 128);
                     if (ostore) tc::mbar_arrive(bar(B_CFREE + e));
@@ -750,7 +757,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 return gt[kGscal + 0];  // e^{g_last} of chunk c
             };
             {  // S from h0 (h0[i][j], i = 64 hh + x)
-#pragma unroll
+#pragma unroll 1
                 for (int part = 0; part < 4; ++part) {
                     uint32_t r[16];
 #pragma unroll
@@ -815,7 +822,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             if (h_T && !*abort_flag && !dead) {
                 tc::tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                 for (int part = 0; part < 4; ++part) {
                     float d[16];
                     tc::tmem_ld16(d2 + 16 * part, d);

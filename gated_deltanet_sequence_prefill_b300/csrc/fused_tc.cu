@@ -119,14 +119,19 @@ __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_fla
 // Bounded mbarrier wait that also stops waiting once the CTA has aborted.
 // Every thread keeps executing the same sequence of named barriers after an
 // abort (work is skipped, barriers are not), so an abort cannot deadlock.
+// The wait is one out-of-line function: inlined at every call site its loop
+// and timeout path made up a large share of the kernel's instruction footprint.
+static __device__ __noinline__ bool wait_bar(volatile int* abort_flag, char* ws, uint32_t bar, uint32_t parity) {
+    if (*abort_flag) return false;
+    if (tc::mbar_wait(bar, parity)) return true;
+    report_timeout(ws, abort_flag);
+    return false;
+}
 struct Waiter {
     volatile int* abort_flag;
     char* ws;
     __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
-        if (*abort_flag) return false;
-        if (tc::mbar_wait(bar, parity)) return true;
-        report_timeout(ws, abort_flag);
-        return false;
+        return wait_bar(abort_flag, ws, bar, parity);
     }
 };
 

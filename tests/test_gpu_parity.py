@@ -108,11 +108,11 @@ def test_gdn_strong_gates(g, scale):
 
 @pytest.mark.parametrize("lengths,h0_std,strong", [([1, 70, 0, 129, 64, 200, 63], 0.01, False),
                                                    ([700, 333], 0.5, True)])
-def test_single_sm_kernel(g, monkeypatch, lengths, h0_std, strong):
-    """The single-SM fused kernel (selected through the environment) against
+def test_pair_kernel(g, monkeypatch, lengths, h0_std, strong):
+    """The 2-SM cluster kernel (selected through the environment) against
     the oracle: ragged sequences, and strong gates that take its unfactored
-    decay path."""
-    monkeypatch.setenv("GDN_PREFILL_SINGLE_SM", "1")
+    decay paths."""
+    monkeypatch.setenv("GDN_PREFILL_PAIR", "1")
     inp = gi.gdn_inputs(lengths, 4, 128, 128, "bf16", h0_std=h0_std, seed=3)
     if strong:
         inp["log_alpha"] = inp["log_alpha"] * 40.0
@@ -178,6 +178,17 @@ def test_gdn_t32768_h16(g):
     inp = gi.gdn_inputs([32768], 16, 128, 128, "bf16", h0_std=0.01, seed=0)
     o, hT = run_gdn(g, inp)
     check_chains(inp, o, hT, [(0, 0), (0, 5), (0, 11), (0, 15)], TOL["bf16"])
+
+
+def test_pair_kernel_varlen_t131072_h32(g, monkeypatch):
+    """The 2-SM cluster kernel on the benchmarked packed call (256 CTAs, more
+    than one wave): 8 sampled chains against the oracle."""
+    monkeypatch.setenv("GDN_PREFILL_PAIR", "1")
+    lengths = gi.varlen_lengths(131072, 4, 0)
+    inp = gi.gdn_inputs(lengths, 32, 128, 128, "bf16", h0_std=0.01, seed=0)
+    o, hT = run_gdn(g, inp)
+    chains = [(0, 0), (0, 31), (1, 5), (2, 17), (3, 9), (3, 30), (1, 22), (2, 2)]
+    check_chains(inp, o, hT, chains, TOL["bf16"])
 
 
 def test_gdn_varlen_t131072_h32(g):
