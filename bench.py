@@ -6,7 +6,7 @@ H = 32 heads, dk = dv = 128, bf16 q/k/v/o, fp32 gates and states, chunk 64
 larger than L2 (4.35 GB), so no L2 flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --workload {gdn_t32768_h16, gdn_t131072_h32_single, linear_b2_t4096_h8,
+  python bench.py --workload {gdn_t32768_h16, gdn_t131072_h32_single, gdn_t65536_h8, linear_b2_t4096_h8,
                               decode_b128_h32}     (the other workloads, one GPU)
 
 One JSON line is printed by rank 0.  Under torchrun each rank runs the same
@@ -27,6 +27,44 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import gdn_inputs as gi  # noqa: E402
+
+KERNEL_SRC = {"fused_single_sm": "fused_tc.cu", "fused_pair": "fused_cluster.cu"}
+
+
+def kernel_name(fused, units=None):
+    """Which prefill kernel gdn_chunk_fwd runs (the library's own dispatch rule:
+    the 2-SM cluster kernel when all (sequence, head) units fit on the GPU as
+    clusters, unless GDN_PREFILL_PAIR forces a choice)."""
+    if not fused:
+        return "staged"
+    env = os.environ.get("GDN_PREFILL_PAIR", "")
+    if env in ("0", "1"):
+        return "fused_pair" if env == "1" else "fused_single_sm"
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return "fused_pair" if units is not None and 2 * units <= sms else "fused_single_sm"
+
+
+def source_digest(kernel):
+    import hashlib
+    path = os.path.join(ROOT, "gated_deltanet_sequence_prefill_b300", "csrc", KERNEL_SRC.get(kernel, ""))
+    if not os.path.isfile(path):
+        return None
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per call from the committed ncu summary, or None when there is
+    none for this kernel or the kernel source changed since it was taken."""
+    prof = os.path.join(ROOT, "profiles", "traffic_gdn_varlen_t131072_h32.json")
+    if not os.path.exists(prof):
+        return None
+    with open(prof) as f:
+        t = json.load(f)
+    if t.get("kernel") != kernel or t.get("source_sha256_16") != source_digest(kernel):
+        return None
+    return t.get("bytes_per_call")
 
 METRIC = "GDN prefill tokens/s at H=32,d=128,T=128K bf16; % of roofline (1×B300)"
 T_TOTAL, H, D = 131072, 32, 128
@@ -284,13 +322,7 @@ def run_ours(args, rank, world, local_rank):
         pk = peaks()
         kern_ms = statistics.median(per_call)
         achieved = alg_bytes() / (kern_ms / 1e3) / 1e9
-        traffic = None
-        prof = os.path.join(ROOT, "profiles", "traffic.json")
-        if os.path.exists(prof):
-            with open(prof) as f:
-                t = json.load(f)
-            if t.get("kernel_set") == ("fused" if fused else "staged"):
-                traffic = t.get("bytes_per_call")
+        traffic = recorded_traffic(kernel_name(fused, n * H))
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -298,7 +330,7 @@ def run_ours(args, rank, world, local_rank):
             "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
                     "log_alpha=-softplus(N)*0.1, beta=sigmoid(N), h0 N(0,0.01))",
             "config": {"workload": WORKLOAD, "T": T, "H": H, "dk": D, "dv": D, "seq_lens": LENGTHS,
-                       "chunk": 64, "path": "fused" if fused else "staged",
+                       "chunk": 64, "path": kernel_name(fused, n * H),
                        "l2": "inputs larger than L2 (%.2f GB per call), no flush" % (alg_bytes() / 1e9)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
                          "frac": achieved / pk["hbm"], "traffic": traffic,
@@ -368,6 +400,9 @@ def run_workload(args):
         elif name == "gdn_t131072_h32_single":
             lengths, Hh, kind = [131072], 32, "gdn"
             inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
+        elif name == "gdn_t65536_h8":  # the small case the ncu summaries capture
+            lengths, Hh, kind = [65536], 8, "gdn"
+            inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
         else:
             raise SystemExit("unknown workload " + name)
         d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
@@ -389,7 +424,7 @@ def run_workload(args):
             (2 if kind == "gdn" else 1) * nn * Hh * D * D * 4
         launches = 2
         cfg = {"workload": name, "T": Tt, "H": Hh, "dk": D, "dv": D, "seq_lens": lengths,
-               "chunk": 64, "l2": ("L2 flushed (256 MB write) between timed calls"
+               "chunk": 64, "path": kernel_name(True, nn * Hh), "l2": ("L2 flushed (256 MB write) between timed calls"
                                    if flush is not None else "inputs larger than L2, no flush")}
     for _ in range(args.warmup):
         run()

@@ -93,11 +93,16 @@ def test_gdn_ragged_varlen(g, dk, dv, dtype, staged):
     assert rel(hT, rh) <= TOL[dtype], rel(hT, rh)
 
 
+KERNELS = [pytest.param("1", id="pair"), pytest.param("0", id="single_sm")]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("scale", [6.0, 40.0])
-def test_gdn_strong_gates(g, scale):
+def test_gdn_strong_gates(g, monkeypatch, kernel, scale):
     """Strongly negative log-decays: a chunk's decay range (about 30 at scale
     6, about 200 at scale 40) straddles or passes the limit of the factored
-    form, so both decay paths of the fused kernel run."""
+    form, so both decay paths of each fused kernel run."""
+    monkeypatch.setenv("GDN_PREFILL_PAIR", kernel)
     inp = gi.gdn_inputs([700, 333, 129], 4, 128, 128, "bf16", h0_std=0.5, seed=5)
     inp["log_alpha"] = inp["log_alpha"] * scale
     o, hT = run_gdn(g, inp)
@@ -106,16 +111,14 @@ def test_gdn_strong_gates(g, scale):
     assert rel(hT, rh) <= TOL["bf16"], rel(hT, rh)
 
 
-@pytest.mark.parametrize("lengths,h0_std,strong", [([1, 70, 0, 129, 64, 200, 63], 0.01, False),
-                                                   ([700, 333], 0.5, True)])
-def test_pair_kernel(g, monkeypatch, lengths, h0_std, strong):
-    """The 2-SM cluster kernel (selected through the environment) against
-    the oracle: ragged sequences, and strong gates that take its unfactored
-    decay paths."""
-    monkeypatch.setenv("GDN_PREFILL_PAIR", "1")
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("lengths,h0_std", [([1, 70, 0, 129, 64, 200, 63], 0.01), ([700, 333], 0.5)])
+def test_fused_kernels(g, monkeypatch, kernel, lengths, h0_std):
+    """Each fused kernel, forced through the environment, against the oracle
+    on ragged packed sequences (the automatic choice picks the cluster kernel
+    for these few units)."""
+    monkeypatch.setenv("GDN_PREFILL_PAIR", kernel)
     inp = gi.gdn_inputs(lengths, 4, 128, 128, "bf16", h0_std=h0_std, seed=3)
-    if strong:
-        inp["log_alpha"] = inp["log_alpha"] * 40.0
     o, hT = run_gdn(g, inp)
     ro, rh = ref_gdn(inp)
     assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
@@ -181,8 +184,8 @@ def test_gdn_t32768_h16(g):
 
 
 def test_pair_kernel_varlen_t131072_h32(g, monkeypatch):
-    """The 2-SM cluster kernel on the benchmarked packed call (256 CTAs, more
-    than one wave): 8 sampled chains against the oracle."""
+    """The 2-SM cluster kernel, forced, on the benchmarked packed call (128
+    clusters, more than fit at once): 8 sampled chains against the oracle."""
     monkeypatch.setenv("GDN_PREFILL_PAIR", "1")
     lengths = gi.varlen_lengths(131072, 4, 0)
     inp = gi.gdn_inputs(lengths, 32, 128, 128, "bf16", h0_std=0.01, seed=0)
