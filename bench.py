@@ -33,16 +33,10 @@ KERNEL_SRC = {"fused_single_sm": "fused_tc.cu", "fused_pair": "fused_cluster.cu"
 
 def kernel_name(fused, units=None):
     """Which prefill kernel gdn_chunk_fwd runs (the library's own dispatch rule:
-    the 2-SM cluster kernel when all (sequence, head) units fit on the GPU as
-    clusters, unless GDN_PREFILL_PAIR forces a choice)."""
+    the 2-SM cluster kernel unless GDN_PREFILL_PAIR=0)."""
     if not fused:
         return "staged"
-    env = os.environ.get("GDN_PREFILL_PAIR", "")
-    if env in ("0", "1"):
-        return "fused_pair" if env == "1" else "fused_single_sm"
-    import torch
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return "fused_pair" if units is not None and 2 * units <= sms else "fused_single_sm"
+    return "fused_single_sm" if os.environ.get("GDN_PREFILL_PAIR", "") == "0" else "fused_pair"
 
 
 def source_digest(kernel):
@@ -402,6 +396,12 @@ def run_workload(args):
             inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
         elif name == "gdn_t65536_h8":  # the small case the ncu summaries capture
             lengths, Hh, kind = [65536], 8, "gdn"
+            inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
+        elif name == "gdn_t16384_h64":  # many concurrent units, small enough for ncu sections
+            lengths, Hh, kind = [16384], 64, "gdn"
+            inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
+        elif name == "gdn_t16384_h4":  # the same length with few units
+            lengths, Hh, kind = [16384], 4, "gdn"
             inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
         else:
             raise SystemExit("unknown workload " + name)

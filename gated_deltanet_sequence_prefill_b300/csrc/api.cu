@@ -77,24 +77,13 @@ PrefillArgs make_args(const void* q, const void* k, const void* v, const float* 
 }
 
 // Which fused kernel: the 2-SM cluster kernel (solve and state pass on
-// separate SMs) when every (sequence, head) unit fits on the GPU at once as a
-// cluster -- its per-chunk period is shorter but grows with the number of busy
-// SMs -- and otherwise the single-SM kernel (one CTA per sequence, head and
-// 64-column half of the state).  GDN_PREFILL_PAIR=1 / =0 in the environment
-// forces one or the other.
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
+// separate SMs) unless GDN_PREFILL_PAIR=0 in the environment selects the
+// single-SM kernel (one CTA per sequence, head and 64-column half of the
+// state).
 bool use_pair(const PrefillArgs& a) {
     if (!pair_supported(a)) return false;
     const char* e = getenv("GDN_PREFILL_PAIR");
-    if (e != nullptr && e[0] == '1') return true;
-    if (e != nullptr && e[0] == '0') return false;
-    return 2LL * a.n_seqs * a.H <= (long long)sm_count();
+    return !(e != nullptr && e[0] == '0');
 }
 
 gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {

@@ -57,7 +57,7 @@ bool encode_gate_map(CUtensorMap* m, const float* ptr, int64_t T, int H);
 
 namespace pair {
 
-constexpr int kThreads = 448;  // 14 warps in both CTAs
+constexpr int kThreads = 480;  // 15 warps in both CTAs
 constexpr int kD = 128;
 
 // ---------------------------------------------------------------- front layout
@@ -201,6 +201,15 @@ __device__ __forceinline__ void store_row64_neg(uint32_t tile, uint32_t r, const
                          tc::pack_bf16(-v[8 * j + 4], -v[8 * j + 5]),
                          tc::pack_bf16(-v[8 * j + 6], -v[8 * j + 7]));
 }
+// An opaque copy of a flag: branching on it inside a loop keeps the compiler
+// from cloning the loop once per flag value (loop unswitching), which would
+// multiply the kernel's instruction footprint.
+__device__ __forceinline__ bool opaque(bool f) {
+    uint32_t v = f;
+    asm volatile("" : "+r"(v));
+    return v != 0;
+}
+
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
@@ -300,11 +309,9 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (tid == 0) {
         *abort_flag = 0;
-        if (front) {
-            for (int b = 0; b < F_COUNT; ++b) tc::mbar_init(bar(b), b == F_FIN ? 4 : 1);
-        } else {
-            for (int b = 0; b < B_COUNT; ++b) tc::mbar_init(bar(b), 1);
-        }
+#pragma unroll 1
+        for (int b = 0; b < (front ? (int)F_COUNT : (int)B_COUNT); ++b)
+            tc::mbar_init(bar(b), (front && b == F_FIN) ? 4 : 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
@@ -338,7 +345,8 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (front) {
         // ============================================================ FRONT
         if (warp == 0) {
-            // ---- TMA, [k; q] k^T, gates (chunk c in stage / group c % 3)
+            // ---- TMA issue only (chunk c in stage c % 3): runs ahead as far as the
+            // ring allows; [k; q] k^T and the gate values are warp 13's
             int issued = 0;
             for (int c = 0; c < nch && !dead; ++c) {
                 const int f = c % kFGroups, uf = c / kFGroups;
@@ -369,25 +377,10 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     }
                 }
                 __syncwarp();
-                wait(bar(F_FULL + f), uf & 1);
-                if (c >= kFGroups) wait(bar(F_P1F + f), (uf - 1) & 1);
-                if (!*abort_flag) {
-                    tc::tc_fence_after();
-                    const uint64_t d0 = tc::sdesc(st + kFK0, 16, 1024), d1 = tc::sdesc(st + kFK0 + kFBlk, 16, 1024);
-                    tc::mma_batch_ss(lane == 0, tmem + kFColP1 + f * 64, d0, 2, d0, 2, kIdP1, 4, false);
-                    tc::mma_batch_ss(lane == 0, tmem + kFColP1 + f * 64, d1, 2, d1, 2, kIdP1, 4, true);
-                    tc::mma_commit_p(lane == 0, bar(F_P1D + f));
-                }
-                const float* la_raw = reinterpret_cast<const float*>(sptr + f * kFStage + kFGRaw);
-                derive_gates<GDN>(la_raw, la_raw + 256, head & 3, min(kChunk, len - c * kChunk),
-                                  reinterpret_cast<float*>(sptr + f * kFStage + kFGate), lane);
-                if (lane == 0) tc::mbar_arrive(bar(F_GREADY + f));
-                __syncwarp();
             }
             if (lane == 0 && *abort_flag)
                 for (int c = max(0, issued - kFGroups); c < issued; ++c)
                     tc::mbar_wait(bar(F_FULL + c % kFGroups), (c / kFGroups) & 1);
-            if (issuer0) tc::mma_commit(bar(F_FIN));
             __syncwarp();
         } else if (warp <= 12) {
             // ---- solve groups: group g takes chunks c with c % 3 == g
@@ -410,56 +403,64 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 const bool safe = gt[kGscal + 1] != 0.f;
                 const int n = (int)gt[kGscal + 2];
                 const int t = row & 63;
+                // rows 0..63: K K^T -> A (fp32); rows 64..127: Q K^T -> P^ (staged, bf16),
+                // in four parts of 16 columns (a short loop keeps this code small).
+                // When the chunk's decay range is moderate, P^ = (q k^T)_causal e^{-g_last};
+                // the back then scales v_new by e^{g_last - g} and o by e^{g}, which gives
+                // the same o and h.
                 {
-                    float x[64];
-                    tc::tmem_ld32(tmem + lane_off + kFColP1 + grp * 64, *reinterpret_cast<float(*)[32]>(x));
-                    tc::tmem_ld32(tmem + lane_off + kFColP1 + grp * 64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-                    tc::tmem_wait_ld();
-                    tc::tc_fence_before();
-                    tc::named_bar(nb, 128);
-                    if (gissuer) tc::mbar_arrive(bar(F_P1F + grp));
-                    __syncwarp();
-                    // rows 0..63: K K^T -> A (fp32); rows 64..127: Q K^T -> P^ (staged, bf16).
-                    // When the chunk's decay range is moderate, P^ = (q k^T)_causal e^{-g_last};
-                    // the back then scales v_new by e^{g_last - g} and o by e^{g}, which gives
-                    // the same o and h.
                     const bool is_a = row < 64;
-                    if (!is_a || GDN) {
-                        const float rs = (is_a ? gt[kGbb + t] : 1.f) * gt[kGeg + t];
-                        const int lim = is_a ? t : t + 1;
-                        const bool tok = t < n;
-                        if (safe && !is_a) {
-                            const float eml = gt[kGscal + 3];
+                    const float rs = (is_a ? gt[kGbb + t] : 1.f) * gt[kGeg + t];
+                    const float eml = gt[kGscal + 3], gtt = gt[kGg + t], bsc = is_a ? gt[kGbb + t] : 1.f;
+                    const int lim = is_a ? t : t + 1;
+                    const bool tok = t < n;
+#pragma unroll 1
+                    for (int part = 0; part < 4; ++part) {
+                        float x[16];
+                        tc::tmem_ld16(tmem + lane_off + kFColP1 + grp * 64 + 16 * part, x);
+                        tc::tmem_wait_ld();
+                        const int s0 = 16 * part;
+                        if (!is_a || GDN) {
+                            if (safe && !is_a) {
 #pragma unroll
-                            for (int sidx = 0; sidx < 64; ++sidx) x[sidx] = (tok && sidx < lim) ? x[sidx] * eml : 0.f;
-                        } else if (safe) {
+                                for (int e2 = 0; e2 < 16; ++e2) x[e2] = (tok && s0 + e2 < lim) ? x[e2] * eml : 0.f;
+                            } else if (safe) {
 #pragma unroll
-                            for (int q4 = 0; q4 < 16; ++q4) {
-                                const float4 en = *reinterpret_cast<const float4*>(gt + kGeng + 4 * q4);
-                                const int s0 = 4 * q4;
-                                x[s0 + 0] = (tok && s0 + 0 < lim) ? x[s0 + 0] * en.x * rs : 0.f;
-                                x[s0 + 1] = (tok && s0 + 1 < lim) ? x[s0 + 1] * en.y * rs : 0.f;
-                                x[s0 + 2] = (tok && s0 + 2 < lim) ? x[s0 + 2] * en.z * rs : 0.f;
-                                x[s0 + 3] = (tok && s0 + 3 < lim) ? x[s0 + 3] * en.w * rs : 0.f;
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    const float4 en = *reinterpret_cast<const float4*>(gt + kGeng + s0 + 4 * q4);
+                                    const int s1 = s0 + 4 * q4;
+                                    x[4 * q4 + 0] = (tok && s1 + 0 < lim) ? x[4 * q4 + 0] * en.x * rs : 0.f;
+                                    x[4 * q4 + 1] = (tok && s1 + 1 < lim) ? x[4 * q4 + 1] * en.y * rs : 0.f;
+                                    x[4 * q4 + 2] = (tok && s1 + 2 < lim) ? x[4 * q4 + 2] * en.z * rs : 0.f;
+                                    x[4 * q4 + 3] = (tok && s1 + 3 < lim) ? x[4 * q4 + 3] * en.w * rs : 0.f;
+                                }
+                            } else {
+#pragma unroll
+                                for (int e2 = 0; e2 < 16; ++e2)
+                                    x[e2] = (tok && s0 + e2 < lim) ? x[e2] * bsc * __expf(gtt - gt[kGg + s0 + e2]) : 0.f;
                             }
-                        } else {
-                            const float gtt = gt[kGg + t], bsc = is_a ? gt[kGbb + t] : 1.f;
+                            if (is_a) {
+                                float* Ar = AF + t * kTriLd + s0;
 #pragma unroll
-                            for (int sidx = 0; sidx < 64; ++sidx)
-                                x[sidx] = (tok && sidx < lim) ? x[sidx] * bsc * __expf(gtt - gt[kGg + sidx]) : 0.f;
-                        }
-                        if (is_a) {
-                            float* Ar = AF + t * kTriLd;
+                                for (int q4 = 0; q4 < 4; ++q4)
+                                    *reinterpret_cast<float4*>(Ar + 4 * q4) =
+                                        make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+                            } else {
 #pragma unroll
-                            for (int q4 = 0; q4 < 16; ++q4)
-                                *reinterpret_cast<float4*>(Ar + 4 * q4) =
-                                    make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
-                        } else {
-                            store_row64(pst, t, x);
+                                for (int h2 = 0; h2 < 2; ++h2)
+                                    tc::st_shared_v4(tc::sw128(pst, t, 2 * part + h2),
+                                                     tc::pack_bf16(x[8 * h2], x[8 * h2 + 1]),
+                                                     tc::pack_bf16(x[8 * h2 + 2], x[8 * h2 + 3]),
+                                                     tc::pack_bf16(x[8 * h2 + 4], x[8 * h2 + 5]),
+                                                     tc::pack_bf16(x[8 * h2 + 6], x[8 * h2 + 7]));
+                            }
                         }
                     }
                 }
-                tc::named_bar(nb, 128);
+                tc::tc_fence_before();
+                tc::named_bar(nb, 128);  // DP1[group] read, A and P^ rows stored
+                if (gissuer) tc::mbar_arrive(bar(F_P1F + grp));
+                __syncwarp();
                 // row t of T diag(cs): T from the inverse (GDN), the identity otherwise
                 auto t_row = [&](const float* cs, float (&v)[64]) {
 #pragma unroll
@@ -554,17 +555,46 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             if (gissuer) tc::mma_commit(bar(F_FIN));  // once its last w MMA is done
             __syncwarp();
+        } else if (warp == 13) {
+            // ---- [k; q] k^T into DP1[c % 3] and the chunk's gate values, as each
+            // chunk lands
+            for (int c = 0; c < nch && !dead; ++c) {
+                const int f = c % kFGroups, uf = c / kFGroups;
+                const uint32_t st = sbase + f * kFStage;
+                wait(bar(F_FULL + f), uf & 1);
+                if (c >= kFGroups) wait(bar(F_P1F + f), (uf - 1) & 1);
+                __syncwarp();
+                if (!*abort_flag) {
+                    tc::tc_fence_after();
+                    const uint64_t d0 = tc::sdesc(st + kFK0, 16, 1024), d1 = tc::sdesc(st + kFK0 + kFBlk, 16, 1024);
+                    tc::mma_batch_ss(lane == 0, tmem + kFColP1 + f * 64, d0, 2, d0, 2, kIdP1, 4, false);
+                    tc::mma_batch_ss(lane == 0, tmem + kFColP1 + f * 64, d1, 2, d1, 2, kIdP1, 4, true);
+                    tc::mma_commit_p(lane == 0, bar(F_P1D + f));
+                }
+                const float* la_raw = reinterpret_cast<const float*>(sptr + f * kFStage + kFGRaw);
+                derive_gates<GDN>(la_raw, la_raw + 256, head & 3, min(kChunk, len - c * kChunk),
+                                  reinterpret_cast<float*>(sptr + f * kFStage + kFGate), lane);
+                if (lane == 0) tc::mbar_arrive(bar(F_GREADY + f));
+                __syncwarp();
+            }
+            tc::mma_commit_p(lane == 0, bar(F_FIN));  // once its last MMA is done
+            __syncwarp();
         }
     } else {
         // ============================================================ BACK
         if (warp == 0) {
-            // ---- TMA into both rings, arming of the push, gates
+            // ---- TMA into both rings and arming of the first pushes (issue only;
+            // warp 14 derives the gate values)
             int issued = 0;
             for (int c = 0; c < nch && !dead; ++c) {
                 const int e = c % 3, a = c & 1;
                 const uint32_t ce = sbase + e * kCEntry, ae = sbase + kARing + a * kAEntry;
                 if (c >= 3) wait(bar(B_CFREE + e), (c / 3 - 1) & 1);
-                if (c >= 2) wait(bar(B_AFREE + a), ((c >> 1) - 1) & 1);
+                if (c >= 2) {
+                    wait(bar(B_AFREE + a), ((c >> 1) - 1) & 1);
+                    // chunk c - 2's raw log-decay in this apply entry has been read
+                    wait(bar(B_GREADY + (c - 2) % 3), ((c - 2) / 3) & 1);
+                }
                 const int t0 = start + c * kChunk;
                 if (lane == 0 && !*abort_flag) {
                     tc::mbar_arrive_expect_tx(bar(B_FULLC + e), 4 * 8192);
@@ -577,12 +607,11 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     tc::tma_load_3d(ae + kAV + kBBox, &tm_v, 64, head, t0, bar(B_FULLA + a));
                     if (GDN) tc::tma_load_2d(ae + kALa, &tm_la, head & ~3, t0, bar(B_FULLA + a));
                     issued = c + 1;
-                    // arm the push of the first three chunks (bytes counted on the chain
-                    // entry) and tell the front; the output warps arm the later ones
-                    if (c < 3) {
-                        tc::mbar_arrive_expect_tx(bar(B_FULLP + e), GDN ? 4 * 8192 : 2 * 8192);
-                        tc::mbar_arrive_remote(peer_bar_f + 8u * (F_ARMED + e));
-                    }
+                    // arm the push of this chunk (bytes counted on the chain entry) and
+                    // tell the front: the entry's -w / P^ and the apply entry's T'' are
+                    // free once CFREE and AFREE above have completed
+                    tc::mbar_arrive_expect_tx(bar(B_FULLP + e), GDN ? 4 * 8192 : 2 * 8192);
+                    tc::mbar_arrive_remote(peer_bar_f + 8u * (F_ARMED + e));
                     if (c + 2 < nch) {
                         const int tp = t0 + 2 * kChunk;
                         tc::tma_prefetch_3d(&tm_v, 0, head, tp);
@@ -590,17 +619,13 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     }
                 }
                 __syncwarp();
-                wait(bar(B_FULLA + a), (c >> 1) & 1);
-                const float* la_raw = reinterpret_cast<const float*>(sptr + kARing + a * kAEntry + kALa);
-                derive_gates<GDN>(la_raw, la_raw, head & 3, min(kChunk, len - c * kChunk),
-                                  reinterpret_cast<float*>(sptr + e * kCEntry + kCGate), lane);
-                if (lane == 0) tc::mbar_arrive(bar(B_GREADY + e));
-                __syncwarp();
             }
+            // after an abort, let the loads already issued land before the CTA exits
+            // (up to three chain entries and two apply entries can be in flight)
             if (lane == 0 && *abort_flag)
-                for (int c = max(0, issued - 2); c < issued; ++c) {
+                for (int c = max(0, issued - 3); c < issued; ++c) {
                     tc::mbar_wait(bar(B_FULLC + c % 3), (c / 3) & 1);
-                    tc::mbar_wait(bar(B_FULLA + (c & 1)), (c >> 1) & 1);
+                    if (c >= issued - 2) tc::mbar_wait(bar(B_FULLA + (c & 1)), (c >> 1) & 1);
                 }
             __syncwarp();
         } else if (warp <= 4) {
@@ -615,51 +640,52 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 wait(bar(B_GREADY + e), (c / 3) & 1);
                 __syncwarp();  // lanes may leave the waits apart; tcgen05.ld is warp-collective
                 tc::tc_fence_after();
-                float x[64];
-                tc::tmem_ld32(tmem + lane_off + kTD1o + 64 * b, *reinterpret_cast<float(*)[32]>(x));
-                tc::tmem_ld32(tmem + lane_off + kTD1o + 64 * b + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-                tc::tmem_wait_ld();
+                const bool fold = gt[kGscal + 1] != 0.f;
+                const int n = min(kChunk, len - c * kChunk);
+                const int t0 = start + c * kChunk;
+                const bool full = n == kChunk;
+                // o = e^g D1o (or D1o) in four parts of 16 tokens: a full chunk is staged
+                // as two [64 t][64 j] SW128 boxes in the k tile (k is dead once D1o is
+                // complete) for two TMA stores; the last, partial chunk of a sequence goes
+                // through fp32 scratch in the same dead entry and plain stores.
+                // Row t = 8u + r of a swizzled box sits at u * 1024 + off[r].
+                const uint32_t box = ce + kCK + (uint32_t)(j >> 6) * kBBox;
+                const uint32_t ch = (uint32_t)(j & 63) >> 3, jj = (uint32_t)(j & 7) * 2;
+                uint32_t off[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) off[r] = box + r * 128 + ((ch ^ r) << 4) + jj;
+                float* xs = reinterpret_cast<float*>(sptr + e * kCEntry + kCK) + j * 65;
+#pragma unroll 1
+                for (int part = 0; part < 4; ++part) {
+                    float x[16];
+                    tc::tmem_ld16(tmem + lane_off + kTD1o + 64 * b + 16 * part, x);
+                    tc::tmem_wait_ld();
+                    if (opaque(fold)) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float4 eg = *reinterpret_cast<const float4*>(gt + kGeg + 16 * part + 4 * q4);
+                            x[4 * q4] *= eg.x;
+                            x[4 * q4 + 1] *= eg.y;
+                            x[4 * q4 + 2] *= eg.z;
+                            x[4 * q4 + 3] *= eg.w;
+                        }
+                    }
+                    if (opaque(full)) {
+#pragma unroll
+                        for (int e2 = 0; e2 < 16; ++e2)
+                            st_shared_u16(off[e2 & 7] + (2 * part + (e2 >> 3)) * 1024,
+                                          __bfloat16_as_ushort(__float2bfloat16_rn(x[e2])));
+                    } else {
+#pragma unroll
+                        for (int e2 = 0; e2 < 16; ++e2) xs[16 * part + e2] = x[e2];
+                    }
+                }
+                tc::fence_proxy_async();
                 tc::tc_fence_before();
                 tc::named_bar(1, 128);
                 if (ostore) {
                     tc::mbar_arrive(bar(B_D1OF + b));
-                    // chunk c's MMAs are done with -w and P^ of this chain entry: arm the
-                    // push of chunk c + 3 once u of chunk c + 1 has also freed its T''
-                    if (c + 3 < nch) {
-                        wait(bar(B_AFREE + ((c + 1) & 1)), ((c + 1) >> 1) & 1);
-                        tc::mbar_arrive_expect_tx(bar(B_FULLP + e), GDN ? 4 * 8192 : 2 * 8192);
-                        tc::mbar_arrive_remote(peer_bar_f + 8u * (F_ARMED + e));
-                    }
-                }
-                __syncwarp();  // lane 0 may have waited above
-                const bool fold = gt[kGscal + 1] != 0.f;
-                const int n = min(kChunk, len - c * kChunk);
-                const int t0 = start + c * kChunk;
-                if (n == kChunk) {
-                    // stage o as two [64 t][64 j] SW128 boxes in the k tile (k is dead
-                    // once D1o is complete), then one TMA store per box.  Row t = 8u + r
-                    // of the swizzled box sits at u * 1024 + off[r].
-                    const uint32_t box = ce + kCK + (uint32_t)(j >> 6) * kBBox;
-                    const uint32_t ch = (uint32_t)(j & 63) >> 3, jj = (uint32_t)(j & 7) * 2;
-                    uint32_t off[8];
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) off[r] = box + r * 128 + ((ch ^ r) << 4) + jj;
-                    if (fold) {
-#pragma unroll
-                        for (int t4 = 0; t4 < 16; ++t4) {
-                            const float4 eg = *reinterpret_cast<const float4*>(gt + kGeg + 4 * t4);
-                            x[4 * t4] *= eg.x;
-                            x[4 * t4 + 1] *= eg.y;
-                            x[4 * t4 + 2] *= eg.z;
-                            x[4 * t4 + 3] *= eg.w;
-                        }
-                    }
-#pragma unroll
-                    for (int t = 0; t < 64; ++t)
-                        st_shared_u16(off[t & 7] + (t >> 3) * 1024, __bfloat16_as_ushort(__float2bfloat16_rn(x[t])));
-                    tc::fence_proxy_async();
-                    tc::named_bar(1, 128);
-                    if (ostore) {
+                    if (full) {
                         if (!*abort_flag) {
                             tc::tma_store_3d(&tm_o, ce + kCK, 0, head, t0);
                             tc::tma_store_3d(&tm_o, ce + kCK + kBBox, 64, head, t0);
@@ -668,19 +694,13 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         tc::bulk_wait_read0();
                         tc::mbar_arrive(bar(B_CFREE + e));
                     }
-                    __syncwarp();
-                } else {
-                    // the sequence's last, partial chunk: plain stores of the valid rows
+                }
+                __syncwarp();
+                if (!full) {
                     if (!*abort_flag) {
-                        // (x is consumed through shared memory so that this rarely
-                        // taken path stays a short loop)
-                        float* xs = reinterpret_cast<float*>(sptr + e * kCEntry + kCK) + j * 65;
-#pragma unroll
-                        for (int t = 0; t < 64; ++t) xs[t] = x[t];
 #pragma unroll 1
                         for (int t = 0; t < n; ++t)
-                            o[((size_t)(t0 + t) * H + head) * kD + j] =
-                                __float2bfloat16_rn(fold ? xs[t] * gt[kGeg + t] : xs[t]);
+                            o[((size_t)(t0 + t) * H + head) * kD + j] = __float2bfloat16_rn(xs[t]);
                     }
                     tc::named_bar(1, 128);
                     if (ostore) tc::mbar_arrive(bar(B_CFREE + e));
@@ -830,6 +850,18 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
                     for (int x = 0; x < 16; ++x) h_T[hbase + (size_t)(64 * hh + 16 * part + x) * kD + j] = d[x];
                 }
+            }
+        } else if (warp == 14) {
+            // ---- the gate values of each chunk, as its log-decay lands
+            for (int c = 0; c < nch && !dead; ++c) {
+                const int e = c % 3, a = c & 1;
+                wait(bar(B_FULLA + a), (c >> 1) & 1);
+                __syncwarp();
+                const float* la_raw = reinterpret_cast<const float*>(sptr + kARing + a * kAEntry + kALa);
+                derive_gates<GDN>(la_raw, la_raw, head & 3, min(kChunk, len - c * kChunk),
+                                  reinterpret_cast<float*>(sptr + e * kCEntry + kCGate), lane);
+                if (lane == 0) tc::mbar_arrive(bar(B_GREADY + e));
+                __syncwarp();
             }
         } else {
             // ---- the MMA warp: every MMA of the back, in chunk order

@@ -211,6 +211,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     if (tid == 0) {
         *abort_flag = 0;
+#pragma unroll 1
         for (int b = 0; b < B_COUNT; ++b) tc::mbar_init(bar(b), b == B_FIN ? 4 : 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&tm_q);

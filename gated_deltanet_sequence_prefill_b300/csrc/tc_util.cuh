@@ -51,7 +51,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false when the bound ran out (the caller reports GDN_ERR_TIMEOUT).
 constexpr int kWaitLimit = 1 << 22;
+// (the polling loops are kept rolled: unrolled, each copy cost kilobytes of
+// instruction footprint)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+#pragma unroll 1
     for (int i = 0; i < kWaitLimit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
@@ -318,6 +321,7 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+#pragma unroll 1
     for (int i = 0; i < kWaitLimit; ++i)
         if (mbar_try_wait_cluster(bar, parity)) return true;
     return false;

@@ -95,11 +95,10 @@ GDN_API size_t gdn_chunk_fwd_workspace_size(int64_t T_total, int H, int dk, int 
  * and "Селектор бюджета по парам голов и компактные снапшоты…" (outputs are
  * produced for every token).  Chunk size 64; chunks restart at every
  * sequence start and the last chunk of a sequence may be partial.
- * For bf16 with dk = dv = 128 the call runs one fused kernel: the one that
- * puts each (sequence, head) on a 2-SM cluster when all of them fit on the GPU
- * at once, otherwise the one with one CTA per (sequence, head, 64-column half
- * of the state).  GDN_PREFILL_PAIR=1 or =0 in the environment forces the
- * first or the second (same results up to rounding).
+ * For bf16 with dk = dv = 128 the call runs one fused kernel that puts each
+ * (sequence, head) on a 2-SM cluster; GDN_PREFILL_PAIR=0 in the environment
+ * selects the kernel with one CTA per (sequence, head, 64-column half of the
+ * state) instead (same results up to rounding).
  */
 GDN_API gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *log_alpha, const float *beta, const float *h0,
