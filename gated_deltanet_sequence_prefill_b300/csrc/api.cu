@@ -89,7 +89,7 @@ bool use_pair(const PrefillArgs& a) {
 gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
     const bool pair = use_pair(a);
     const bool fused = pair || fused_supported(a);
-    size_t need = plan_bytes(a.n_seqs);
+    size_t need = pair ? pair_workspace_bytes(a.n_seqs, a.H) : plan_bytes(a.n_seqs);
     if (!fused) need += staged_intermediate_bytes(a.T_total, a.H, a.dk, a.dv, a.n_seqs);
     gdn_status s = check_prefill(a, ws_bytes, need, true);
     if (s != GDN_OK) return s;
@@ -130,6 +130,7 @@ size_t gdn_chunk_fwd_workspace_size(int64_t T, int H, int dk, int dv, int n_seqs
     if (!sizes_ok(T, H, dk, dv, n_seqs) || (io != GDN_BF16 && io != GDN_FP32)) return 0;
     PrefillArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, n_seqs,
                               T, H, dk, dv, io, true, nullptr, nullptr, nullptr);
+    if (pair_shape_ok(a)) return pair_workspace_bytes(n_seqs, H);
     if (fused_supported(a)) return plan_bytes(n_seqs);
     return gdn_staged_workspace_size(T, H, dk, dv, n_seqs, io);
 }
@@ -138,6 +139,7 @@ size_t linear_attn_fwd_workspace_size(int64_t T, int H, int dk, int dv, int n_se
     if (!sizes_ok(T, H, dk, dv, n_seqs) || (io != GDN_BF16 && io != GDN_FP32)) return 0;
     PrefillArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, n_seqs,
                               T, H, dk, dv, io, false, nullptr, nullptr, nullptr);
+    if (pair_shape_ok(a)) return pair_workspace_bytes(n_seqs, H);
     if (fused_supported(a)) return plan_bytes(n_seqs);
     return gdn_staged_workspace_size(T, H, dk, dv, n_seqs, io);
 }

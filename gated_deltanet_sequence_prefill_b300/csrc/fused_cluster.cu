@@ -57,7 +57,7 @@ bool encode_gate_map(CUtensorMap* m, const float* ptr, int64_t T, int H);
 
 namespace pair {
 
-constexpr int kThreads = 480;  // 15 warps in both CTAs
+constexpr int kThreads = 512;  // 16 warps in both CTAs
 constexpr int kD = 128;
 
 // ---------------------------------------------------------------- front layout
@@ -66,13 +66,17 @@ constexpr uint32_t kFBlk = 16384;                                         // K-b
 constexpr uint32_t kFGRaw = 32768;                                        // la [64][4], beta [64][4]
 constexpr uint32_t kFGate = 34816;                                        // derived gate arrays
 constexpr uint32_t kFStage = 36864;
-constexpr int kFGroups = 3;                                // = ring stages: chunk c uses both c % 3
-constexpr uint32_t kFPst = kFGroups * kFStage;             // 3 x P^ staging (bf16 64x64, swizzled)
-constexpr uint32_t kFT1 = kFPst + kFGroups * 8192;         // 3 x T' (bf16 64x64, K-major B operand)
-constexpr uint32_t kFAF = kFT1 + kFGroups * 8192;          // 3 x A/T fp32 [64][68]
+constexpr int kFGroups = 3;   // solve groups: chunk c goes to group c % 3
+constexpr int kFStages = 4;   // TMA stages: chunk c lands in stage c % 4 (one chunk of lookahead)
+// Once [k; q] k^T is done the stage's q tile is dead: its first box then holds
+// T' = T diag(beta e^g) (the B operand of the w MMA), its second T'' = T diag(beta).
+constexpr uint32_t kFT1 = kFQ0, kFT2 = kFQ1;
+constexpr uint32_t kFPst = kFStages * kFStage;             // 3 x P^ staging (bf16 64x64, swizzled)
+constexpr uint32_t kFAF = kFPst + kFGroups * 8192;         // 3 x A/T fp32 [64][68]; later -w staging
 constexpr uint32_t kFScr = kFAF + kFGroups * 64 * kTriLd * 4;  // 3 x 4 x 128 floats
+constexpr int kBarSlots = 40;
 constexpr uint32_t kFBar = kFScr + kFGroups * 4 * 128 * 4;
-constexpr uint32_t kFEnd = kFBar + 32 * 8 + 64;
+constexpr uint32_t kFEnd = kFBar + kBarSlots * 8 + 64;
 
 // ---------------------------------------------------------------- back layout
 // Chain ring (3 entries, chunk c in entry c % 3): q and k as two 64-column
@@ -87,31 +91,39 @@ constexpr uint32_t kARing = 3 * kCEntry;
 constexpr uint32_t kAV = 0, kAT2 = 16384, kALa = 24576;
 constexpr uint32_t kAEntry = 25600;
 constexpr uint32_t kBBar = kARing + 2 * kAEntry;
-constexpr uint32_t kBEnd = kBBar + 32 * 8 + 64;
+constexpr uint32_t kBEnd = kBBar + kBarSlots * 8 + 64;
+
+// Global scratch per (sequence, head): six 32 KB slots (chunk c in slot c % 6)
+// holding P^ [64 t][64 s], T'' [64 t][64 s] and -w [128 i][64 t] (bf16, rows of
+// 128 bytes already in the 128-byte swizzle of the state CTA's tiles).
+constexpr int kSlots = 6;
+constexpr uint32_t kScratchSlot = 32768;
+constexpr uint32_t kScratchUnit = kSlots * kScratchSlot;
 
 constexpr uint32_t kSmemBytes = (kFEnd > kBEnd ? kFEnd : kBEnd);
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
-static_assert(kFBar + 32 * 8 <= kSmemBytes && kBBar + 32 * 8 <= kSmemBytes, "barriers");
+static_assert(kFBar + kBarSlots * 8 <= kSmemBytes && kBBar + kBarSlots * 8 <= kSmemBytes, "barriers");
 static_assert(kCEntry % 1024 == 0 && kARing % 1024 == 0 && kAEntry % 1024 == 0, "tile alignment");
 
 // gate arrays (float index from the gate area); scalars at kGscal:
-// [0] e^{g_last}, [1] safe-factor flag, [2] n valid, [3] e^{-g_last}
-constexpr int kGg = 0, kGeg = 64, kGeng = 128, kGbeg = 192, kGbb = 256, kGkdec = 320, kGscal = 384;
+// [0] e^{g_last}, [1] safe-factor flag, [2] n valid, [3] e^{-g_last}; kGone holds ones
+constexpr int kGg = 0, kGeg = 64, kGeng = 128, kGbeg = 192, kGbb = 256, kGkdec = 320, kGscal = 384, kGone = 448;
 
 // ---------------------------------------------------------------- barriers
 // front
 enum {
-    F_FULL = 0,     // [3] TMA landed
-    F_GREADY = 3,   // [3] gate values derived
-    F_EMPTY = 6,    // [3] stage free
-    F_P1D = 9,      // [3] [k;q]k^T done in DP1[group]
-    F_P1F = 12,     // [3] DP1[group] read
-    F_ARMED = 15,   // [3] back chain entry armed for this chunk  (remote arrive by the back)
-    F_PUSHED = 18,  // [3] group pushed its chunk (orders the pushes of the three groups)
-    F_WD = 21,      // [3] w^T MMA of the group done
-    F_FIN = 24,
-    F_COUNT = 25
+    F_FULL = 0,     // [4] TMA landed in stage c % 4
+    F_EMPTY = 4,    // [4] stage free (a store warp has read T'' out of it)
+    F_GREADY = 8,   // [3] gate values of the group's chunk derived
+    F_P1D = 11,     // [3] [k;q]k^T done in DP1[group]
+    F_P1F = 14,     // [3] DP1[group] read
+    F_STAGED = 17,  // [3] group staged P^, T'', -w of its chunk for the store warps
+    F_WD = 20,      // [3] w^T MMA of the group done
+    F_FIN = 23,
+    F_SFREE = 24,   // [3] a store warp has read the group's staging (P^, -w in AF)
+    F_ARMED = 27,   // [6] scratch slot read by the state CTA (remote arrive by the back)
+    F_COUNT = 33
 };
 // back
 enum {
@@ -128,7 +140,8 @@ enum {
     B_SREADY = 22,  // S (bf16) of the next chunk in TMEM (chain -> issuer)
     B_VREADY = 23,  // v^ in TMEM (chain -> issuer)
     B_FIN = 24,
-    B_COUNT = 25
+    B_STORED = 25,  // [6] the solve CTA's chunk is in its global scratch slot (remote arrive)
+    B_COUNT = 31
 };
 
 // TMEM columns
@@ -184,23 +197,6 @@ struct Waiter {
     }
 };
 
-__device__ __forceinline__ void store_row64(uint32_t tile, uint32_t r, const float* v) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        tc::st_shared_v4(tc::sw128(tile, r, j), tc::pack_bf16(v[8 * j], v[8 * j + 1]),
-                         tc::pack_bf16(v[8 * j + 2], v[8 * j + 3]),
-                         tc::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                         tc::pack_bf16(v[8 * j + 6], v[8 * j + 7]));
-}
-// -v as one bf16 row of a 128-byte-swizzled tile.
-__device__ __forceinline__ void store_row64_neg(uint32_t tile, uint32_t r, const float* v) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        tc::st_shared_v4(tc::sw128(tile, r, j), tc::pack_bf16(-v[8 * j], -v[8 * j + 1]),
-                         tc::pack_bf16(-v[8 * j + 2], -v[8 * j + 3]),
-                         tc::pack_bf16(-v[8 * j + 4], -v[8 * j + 5]),
-                         tc::pack_bf16(-v[8 * j + 6], -v[8 * j + 7]));
-}
 // An opaque copy of a flag: branching on it inside a loop keeps the compiler
 // from cloning the loop once per flag value (loop unswitching), which would
 // multiply the kernel's instruction footprint.
@@ -256,6 +252,8 @@ __device__ __noinline__ void derive_gates(const float* la_raw, const float* b_ra
     gt[kGbb + tb] = bb;
     gt[kGkdec + ta] = ta < n ? __expf(glast - ga) : 0.f;
     gt[kGkdec + tb] = tb < n ? __expf(glast - gb) : 0.f;
+    gt[kGone + ta] = 1.f;
+    gt[kGone + tb] = 1.f;
     if (lane == 0) {
         gt[kGscal + 0] = __expf(glast);
         gt[kGscal + 1] = amax <= 40.f ? 1.f : 0.f;
@@ -271,7 +269,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
             const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_o,
             const float* __restrict__ h0, __nv_bfloat16* __restrict__ o, float* __restrict__ h_T,
-            char* __restrict__ ws, int H) {
+            char* __restrict__ ws, char* __restrict__ scratch, int H) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -303,8 +301,8 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     const uint32_t bar_base = sbase + (front ? kFBar : kBBar);
     auto bar = [&](int i) { return bar_base + 8u * (uint32_t)i; };
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + (front ? kFBar : kBBar) + 32 * 8);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (front ? kFBar : kBBar) + 32 * 8 + 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + (front ? kFBar : kBBar) + kBarSlots * 8);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (front ? kFBar : kBBar) + kBarSlots * 8 + 8);
     const Waiter wait{abort_flag, ws, bar_base, front ? 1000 : 2000};
 
     if (tid == 0) {
@@ -325,7 +323,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
     }
     __syncwarp();  // lane-0-only work above: reconverge before any .aligned instruction
-    if (warp == 0) tc::tmem_alloc(sbase + (front ? kFBar : kBBar) + 32 * 8 + 8, front ? kFTmemCols : kBTmemCols);
+    if (warp == 0) tc::tmem_alloc(sbase + (front ? kFBar : kBBar) + kBarSlots * 8 + 8, front ? kFTmemCols : kBTmemCols);
     tc::tc_fence_before();
     __syncthreads();
     tc::cluster_sync();  // both CTAs' barriers exist before any remote access
@@ -340,7 +338,6 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t peer_bar_b = peer_base + kBBar;
     const uint32_t peer_bar_f = tc::map_to_rank(sbase + kFBar, 0);  // front barriers, seen from the back
 
-    const bool issuer0 = (warp == 0 && lane == 0);
 
     if (front) {
         // ============================================================ FRONT
@@ -349,9 +346,9 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             // ring allows; [k; q] k^T and the gate values are warp 13's
             int issued = 0;
             for (int c = 0; c < nch && !dead; ++c) {
-                const int f = c % kFGroups, uf = c / kFGroups;
+                const int f = c % kFStages, uf = c / kFStages;
                 const uint32_t st = sbase + f * kFStage;
-                if (c >= kFGroups) wait(bar(F_EMPTY + f), (uf - 1) & 1);
+                if (c >= kFStages) wait(bar(F_EMPTY + f), (uf - 1) & 1);
                 const int t0 = start + c * kChunk;
                 if (lane == 0 && !*abort_flag) {
                     tc::mbar_arrive_expect_tx(bar(F_FULL + f), 32768 + (GDN ? 2048 : 0));
@@ -379,8 +376,8 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 __syncwarp();
             }
             if (lane == 0 && *abort_flag)
-                for (int c = max(0, issued - kFGroups); c < issued; ++c)
-                    tc::mbar_wait(bar(F_FULL + c % kFGroups), (c / kFGroups) & 1);
+                for (int c = max(0, issued - kFStages); c < issued; ++c)
+                    tc::mbar_wait(bar(F_FULL + c % kFStages), (c / kFStages) & 1);
             __syncwarp();
         } else if (warp <= 12) {
             // ---- solve groups: group g takes chunks c with c % 3 == g
@@ -391,15 +388,17 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             float* AF = reinterpret_cast<float*>(sptr + kFAF + grp * 64 * kTriLd * 4);
             float* scr = reinterpret_cast<float*>(sptr + kFScr + grp * 4 * 128 * 4);
             const uint32_t pst = sbase + kFPst + grp * 8192;
-            const uint32_t t1s = sbase + kFT1 + grp * 8192;
-            const uint32_t stg = sbase + grp * kFStage;
             for (int c = grp; c < nch && !dead; c += kFGroups) {
-                const int uf = c / kFGroups, e = c % 3, a = c & 1;
+                const int uf = c / kFGroups;
+                const uint32_t stg = sbase + (c % kFStages) * kFStage;
                 wait(bar(F_GREADY + grp), uf & 1);
                 wait(bar(F_P1D + grp), uf & 1);
+                // P^ staging and AF are rewritten below: the store warp must have read
+                // this group's previous chunk out of them
+                if (c >= kFGroups) wait(bar(F_SFREE + grp), (uf - 1) & 1);
                 __syncwarp();
                 tc::tc_fence_after();
-                const float* gt = reinterpret_cast<const float*>(sptr + grp * kFStage + kFGate);
+                const float* gt = reinterpret_cast<const float*>(sptr + (c % kFStages) * kFStage + kFGate);
                 const bool safe = gt[kGscal + 1] != 0.f;
                 const int n = (int)gt[kGscal + 2];
                 const int t = row & 63;
@@ -410,8 +409,10 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 // the same o and h.
                 {
                     const bool is_a = row < 64;
-                    const float rs = (is_a ? gt[kGbb + t] : 1.f) * gt[kGeg + t];
-                    const float eml = gt[kGscal + 3], gtt = gt[kGg + t], bsc = is_a ? gt[kGbb + t] : 1.f;
+                    // safe factors: A[t][s] = KK[t][s] beta_t e^{g_t} e^{-g_s}, P^[t][s] = QK[t][s] e^{-g_last}
+                    const float rs = is_a ? gt[kGbb + t] * gt[kGeg + t] : gt[kGscal + 3];
+                    const float* const en = gt + (is_a ? kGeng : kGone);
+                    const float gtt = gt[kGg + t], bsc = is_a ? gt[kGbb + t] : 1.f;
                     const int lim = is_a ? t : t + 1;
                     const bool tok = t < n;
 #pragma unroll 1
@@ -421,18 +422,15 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         tc::tmem_wait_ld();
                         const int s0 = 16 * part;
                         if (!is_a || GDN) {
-                            if (safe && !is_a) {
-#pragma unroll
-                                for (int e2 = 0; e2 < 16; ++e2) x[e2] = (tok && s0 + e2 < lim) ? x[e2] * eml : 0.f;
-                            } else if (safe) {
+                            if (safe) {
 #pragma unroll
                                 for (int q4 = 0; q4 < 4; ++q4) {
-                                    const float4 en = *reinterpret_cast<const float4*>(gt + kGeng + s0 + 4 * q4);
+                                    const float4 f = *reinterpret_cast<const float4*>(en + s0 + 4 * q4);
                                     const int s1 = s0 + 4 * q4;
-                                    x[4 * q4 + 0] = (tok && s1 + 0 < lim) ? x[4 * q4 + 0] * en.x * rs : 0.f;
-                                    x[4 * q4 + 1] = (tok && s1 + 1 < lim) ? x[4 * q4 + 1] * en.y * rs : 0.f;
-                                    x[4 * q4 + 2] = (tok && s1 + 2 < lim) ? x[4 * q4 + 2] * en.z * rs : 0.f;
-                                    x[4 * q4 + 3] = (tok && s1 + 3 < lim) ? x[4 * q4 + 3] * en.w * rs : 0.f;
+                                    x[4 * q4 + 0] = (tok && s1 + 0 < lim) ? x[4 * q4 + 0] * f.x * rs : 0.f;
+                                    x[4 * q4 + 1] = (tok && s1 + 1 < lim) ? x[4 * q4 + 1] * f.y * rs : 0.f;
+                                    x[4 * q4 + 2] = (tok && s1 + 2 < lim) ? x[4 * q4 + 2] * f.z * rs : 0.f;
+                                    x[4 * q4 + 3] = (tok && s1 + 3 < lim) ? x[4 * q4 + 3] * f.w * rs : 0.f;
                                 }
                             } else {
 #pragma unroll
@@ -461,124 +459,135 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tc::named_bar(nb, 128);  // DP1[group] read, A and P^ rows stored
                 if (gissuer) tc::mbar_arrive(bar(F_P1F + grp));
                 __syncwarp();
-                // row t of T diag(cs): T from the inverse (GDN), the identity otherwise
-                auto t_row = [&](const float* cs, float (&v)[64]) {
-#pragma unroll
+                if (GDN) tri_inverse_64(AF, scr, pw, lane, nb);
+                // T' = T diag(beta e^g) (bf16, K-major) for w^T = k^T T'^T on this SM (rows
+                // 0..63), and T'' = T diag(beta) for the state CTA's u MMA (rows 64..127),
+                // both into the stage's dead q tile, 16 columns at a time.  T is the inverse
+                // (GDN) or the identity.
+                {
+                    const float* cs = gt + (row < 64 ? kGbeg : kGbb);
+                    const uint32_t dst = stg + (row < 64 ? kFT1 : kFT2);
+#pragma unroll 1
                     for (int jb = 0; jb < 4; ++jb) {
+                        float v[16];
                         if (GDN && jb <= (t >> 4)) {
                             const float* Tr = tri_block_row(AF, t, jb);
 #pragma unroll
                             for (int e4 = 0; e4 < 16; e4 += 4) {
                                 const float4 tv = *reinterpret_cast<const float4*>(Tr + e4);
                                 const float4 sv = *reinterpret_cast<const float4*>(cs + 16 * jb + e4);
-                                v[16 * jb + e4] = tv.x * sv.x;
-                                v[16 * jb + e4 + 1] = tv.y * sv.y;
-                                v[16 * jb + e4 + 2] = tv.z * sv.z;
-                                v[16 * jb + e4 + 3] = tv.w * sv.w;
+                                v[e4] = tv.x * sv.x;
+                                v[e4 + 1] = tv.y * sv.y;
+                                v[e4 + 2] = tv.z * sv.z;
+                                v[e4 + 3] = tv.w * sv.w;
                             }
                         } else {
 #pragma unroll
-                            for (int e4 = 0; e4 < 16; ++e4) v[16 * jb + e4] = (!GDN && 16 * jb + e4 == t) ? cs[t] : 0.f;
+                            for (int e4 = 0; e4 < 16; ++e4) v[e4] = (!GDN && 16 * jb + e4 == t) ? cs[t] : 0.f;
                         }
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2)
+                            tc::st_shared_v4(tc::sw128(dst, t, 2 * jb + h2), tc::pack_bf16(v[8 * h2], v[8 * h2 + 1]),
+                                             tc::pack_bf16(v[8 * h2 + 2], v[8 * h2 + 3]),
+                                             tc::pack_bf16(v[8 * h2 + 4], v[8 * h2 + 5]),
+                                             tc::pack_bf16(v[8 * h2 + 6], v[8 * h2 + 7]));
                     }
-                };
+                }
+                tc::fence_proxy_async();
+                tc::tc_fence_before();
+                tc::named_bar(nb, 128);  // T' and T'' staged; AF (T) is dead
                 if (GDN) {
-                    tri_inverse_64(AF, scr, pw, lane, nb);
-                    // T' = T diag(beta e^g) (bf16, K-major) for w^T = k^T T'^T on this SM
-                    if (row < 64) {
-                        float v[64];
-                        t_row(gt + kGbeg, v);
-                        store_row64(t1s, t, v);
-                    }
-                    tc::fence_proxy_async();
-                    tc::tc_fence_before();
-                    tc::named_bar(nb, 128);
                     if (pw == 3 && !*abort_flag) {
                         tc::tc_fence_after();
-                        tc::mma_batch_ss(lane == 0, tmem + kFColW + 64 * grp, tc::sdesc(stg + kFK0, kFBlk, 1024), 128,
-                                         tc::sdesc(t1s, 16, 1024), 2, kIdWU, 4, false);
-                        tc::mma_commit_p(lane == 0, bar(F_WD + grp));
+                        tc::mma_ss_n<4>(tmem + kFColW + 64 * grp, tc::sdesc(stg + kFK0, kFBlk, 1024), 128,
+                                        tc::sdesc(stg + kFT1, 16, 1024), 2, kIdWU, false);
+                        tc::commit_e(bar(F_WD + grp));
                     }
                     __syncwarp();
-                }
-                // ---- push -w, P^ (chain entry c % 3) and T'' = T diag(beta) (apply entry
-                // c % 2) in chunk order, once the back has armed them (the bytes are counted
-                // on the chain entry's barrier).  Waiting for chunk c - 1's push first keeps
-                // the parity wait below at most one phase behind.
-                if (c >= 1) wait(bar(F_PUSHED + (c - 1) % kFGroups), ((c - 1) / kFGroups) & 1);
-                wait.remote(bar(F_ARMED + e), (c / 3) & 1);
-                if (!*abort_flag) {
-                    const uint32_t fb = peer_bar_b + 8u * (B_FULLP + e);
-                    const uint32_t centry = peer_base + e * kCEntry;
-                    if (row >= 64) {
+                    // -w row i = row, as [i][t] (the MN-major B operand of the state CTA's
+                    // w MMA), staged in AF
+                    wait(bar(F_WD + grp), uf & 1);
+                    __syncwarp();
+                    tc::tc_fence_after();
+                    const uint32_t wst = sbase + kFAF + grp * 64 * kTriLd * 4;
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        float x[32];
+                        tc::tmem_ld32(tmem + lane_off + kFColW + 64 * grp + 32 * half, x);
+                        tc::tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint4 pv = tc::ld_shared_v4(tc::sw128(pst, t, j));
-                            tc::st_async_v4(tc::sw128(centry + kCP, t, j), pv.x, pv.y, pv.z, pv.w, fb);
-                        }
-                        float v[64];
-                        t_row(gt + kGbb, v);
-                        const uint32_t t2 = peer_base + kARing + a * kAEntry + kAT2;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            tc::st_async_v4(tc::sw128(t2, t, j), tc::pack_bf16(v[8 * j], v[8 * j + 1]),
-                                            tc::pack_bf16(v[8 * j + 2], v[8 * j + 3]),
-                                            tc::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
-                                            tc::pack_bf16(v[8 * j + 6], v[8 * j + 7]), fb);
+                        for (int j = 0; j < 4; ++j)
+                            tc::st_shared_v4(tc::sw128(wst, row, 4 * half + j), tc::pack_bf16(-x[8 * j], -x[8 * j + 1]),
+                                             tc::pack_bf16(-x[8 * j + 2], -x[8 * j + 3]),
+                                             tc::pack_bf16(-x[8 * j + 4], -x[8 * j + 5]),
+                                             tc::pack_bf16(-x[8 * j + 6], -x[8 * j + 7]));
                     }
-                    if (GDN) {  // -w row i = row, as [i][t]
-                        wait(bar(F_WD + grp), uf & 1);
-                        __syncwarp();
-                        tc::tc_fence_after();
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            float x[32];
-                            tc::tmem_ld32(tmem + lane_off + kFColW + 64 * grp + 32 * half, x);
-                            tc::tmem_wait_ld();
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                tc::st_async_v4(tc::sw128(centry + kCW, row, 4 * half + j),
-                                                tc::pack_bf16(-x[8 * j], -x[8 * j + 1]),
-                                                tc::pack_bf16(-x[8 * j + 2], -x[8 * j + 3]),
-                                                tc::pack_bf16(-x[8 * j + 4], -x[8 * j + 5]),
-                                                tc::pack_bf16(-x[8 * j + 6], -x[8 * j + 7]), fb);
-                        }
-                    }
+                    tc::fence_proxy_async();
                 }
                 tc::tc_fence_before();
-                tc::named_bar(nb, 128);  // AF, the stagings, DW and the stage are free
-                if (gissuer) {
-                    tc::mbar_arrive(bar(F_PUSHED + grp));
-                    tc::mbar_arrive(bar(F_EMPTY + grp));
-                }
+                tc::named_bar(nb, 128);  // P^, T'' and -w staged for the store warp
+                if (gissuer) tc::mbar_arrive(bar(F_STAGED + grp));
                 __syncwarp();
             }
-            if (gissuer) tc::mma_commit(bar(F_FIN));  // once its last w MMA is done
+            if (pw == 3) tc::commit_e(bar(F_FIN));  // once its last w MMA is done
             __syncwarp();
         } else if (warp == 13) {
             // ---- [k; q] k^T into DP1[c % 3] and the chunk's gate values, as each
             // chunk lands
             for (int c = 0; c < nch && !dead; ++c) {
-                const int f = c % kFGroups, uf = c / kFGroups;
+                const int f = c % kFStages, g = c % kFGroups, ug = c / kFGroups;
                 const uint32_t st = sbase + f * kFStage;
-                wait(bar(F_FULL + f), uf & 1);
-                if (c >= kFGroups) wait(bar(F_P1F + f), (uf - 1) & 1);
+                wait(bar(F_FULL + f), (c / kFStages) & 1);
+                if (c >= kFGroups) wait(bar(F_P1F + g), (ug - 1) & 1);
                 __syncwarp();
                 if (!*abort_flag) {
                     tc::tc_fence_after();
                     const uint64_t d0 = tc::sdesc(st + kFK0, 16, 1024), d1 = tc::sdesc(st + kFK0 + kFBlk, 16, 1024);
-                    tc::mma_batch_ss(lane == 0, tmem + kFColP1 + f * 64, d0, 2, d0, 2, kIdP1, 4, false);
-                    tc::mma_batch_ss(lane == 0, tmem + kFColP1 + f * 64, d1, 2, d1, 2, kIdP1, 4, true);
-                    tc::mma_commit_p(lane == 0, bar(F_P1D + f));
+                    tc::mma_ss_n<4>(tmem + kFColP1 + g * 64, d0, 2, d0, 2, kIdP1, false);
+                    tc::mma_ss_n<4>(tmem + kFColP1 + g * 64, d1, 2, d1, 2, kIdP1, true);
+                    tc::commit_e(bar(F_P1D + g));
                 }
                 const float* la_raw = reinterpret_cast<const float*>(sptr + f * kFStage + kFGRaw);
                 derive_gates<GDN>(la_raw, la_raw + 256, head & 3, min(kChunk, len - c * kChunk),
                                   reinterpret_cast<float*>(sptr + f * kFStage + kFGate), lane);
-                if (lane == 0) tc::mbar_arrive(bar(F_GREADY + f));
+                if (lane == 0) tc::mbar_arrive(bar(F_GREADY + g));
                 __syncwarp();
             }
-            tc::mma_commit_p(lane == 0, bar(F_FIN));  // once its last MMA is done
+            tc::commit_e(bar(F_FIN));  // once its last MMA is done
             __syncwarp();
+        } else if (warp >= 14) {
+            // ---- store warps (14: even chunks, 15: odd chunks): each chunk's P^, T'' and
+            // -w go from the group's staging to this unit's global scratch slot c % 6
+            // (bulk copies through L2; the state CTA loads them from there) and are
+            // announced once written.  A slot is rewritten only after the state CTA has
+            // read the chunk it held before.
+            char* const slot0 = scratch + (size_t)unit * kScratchUnit;
+            for (int c = warp - 14; c < nch && !dead; c += 2) {
+                const int grp = c % kFGroups, uf = c / kFGroups, sl = c % kSlots;
+                wait(bar(F_STAGED + grp), uf & 1);
+                if (c >= kSlots) wait.remote(bar(F_ARMED + sl), (c / kSlots - 1) & 1);
+                __syncwarp();
+                if (lane == 0) {
+                    const bool go = !*abort_flag;
+                    if (go) {
+                        char* const slot = slot0 + sl * kScratchSlot;
+                        tc::bulk_store(slot, sbase + kFPst + grp * 8192, 8192);
+                        tc::bulk_store(slot + 8192, sbase + (c % kFStages) * kFStage + kFT2, 8192);
+                        if (GDN) tc::bulk_store(slot + 16384, sbase + kFAF + grp * 64 * kTriLd * 4, 16384);
+                        tc::bulk_commit();
+                        tc::bulk_wait_read0();
+                    }
+                    tc::mbar_arrive(bar(F_SFREE + grp));  // the staging and the stage may be reused
+                    tc::mbar_arrive(bar(F_EMPTY + c % kFStages));
+                    if (go) {  // the slot's writes are done: tell the state CTA
+                        tc::bulk_wait0();
+                        tc::fence_proxy_async_global();
+                        tc::fence_acq_rel_gpu();
+                        tc::mbar_arrive_remote(peer_bar_b + 8u * (B_STORED + sl));
+                    }
+                }
+                __syncwarp();
+            }
         }
     } else {
         // ============================================================ BACK
@@ -607,11 +616,6 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     tc::tma_load_3d(ae + kAV + kBBox, &tm_v, 64, head, t0, bar(B_FULLA + a));
                     if (GDN) tc::tma_load_2d(ae + kALa, &tm_la, head & ~3, t0, bar(B_FULLA + a));
                     issued = c + 1;
-                    // arm the push of this chunk (bytes counted on the chain entry) and
-                    // tell the front: the entry's -w / P^ and the apply entry's T'' are
-                    // free once CFREE and AFREE above have completed
-                    tc::mbar_arrive_expect_tx(bar(B_FULLP + e), GDN ? 4 * 8192 : 2 * 8192);
-                    tc::mbar_arrive_remote(peer_bar_f + 8u * (F_ARMED + e));
                     if (c + 2 < nch) {
                         const int tp = t0 + 2 * kChunk;
                         tc::tma_prefetch_3d(&tm_v, 0, head, tp);
@@ -723,7 +727,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const uint32_t ts = tmem + lane_off + kTS + 32 * hh;
             // S (bf16) <- S (fp32)
             auto snapshot = [&]() {
-#pragma unroll
+#pragma unroll 1
                 for (int part = 0; part < 2; ++part) {
                     float d[32];
                     tc::tmem_ld32(d2 + 32 * part, d);
@@ -737,7 +741,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             };
             // S (fp32) *= f
             auto decay = [&](float f) {
-#pragma unroll
+#pragma unroll 1
                 for (int part = 0; part < 4; ++part) {
                     float d[16];
                     tc::tmem_ld16(d2 + 16 * part, d);
@@ -787,46 +791,43 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
                 tc::tmem_wait_st();
             }
-            snapshot();
-            if (nch > 0 && !dead) {
-                const float egl0 = prescale(0);
-                if (GDN) decay(egl0);
-            }
-            tc::tc_fence_before();
-            tc::named_bar(2, 256);
-            if (cl) tc::mbar_arrive(bar(B_SREADY));
-            __syncwarp();
-            for (int c = 0; c < nch && !dead; ++c) {
-                const int e = c % 3, b = c & 1;
-                const float* gt = reinterpret_cast<const float*>(sptr + e * kCEntry + kCGate);
-                // (1) v^ = e^{g_last - g} v_new (or v_new), bf16 into TMEM
-                wait(bar(B_GREADY + e), (c / 3) & 1);
-                wait(bar(B_M1W), c & 1);
-                __syncwarp();
-                tc::tc_fence_after();
-                const bool fold = gt[kGscal + 1] != 0.f;
-                {
-                    float x[32];
-                    tc::tmem_ld32(tmem + lane_off + kTD1v + 64 * b + 32 * hh, x);
-                    tc::tmem_wait_ld();
-                    uint32_t pk[16];
+            // c = -1 only prepares chunk 0: S (bf16) from h0, the gates of chunk 0, the
+            // decay of S (fp32) for chunk 0; every later pass first finishes chunk c.
+            // (One copy of each step keeps this warp's instruction footprint small.)
+            for (int c = -1; c < nch && !dead; ++c) {
+                if (c >= 0) {
+                    const int e = c % 3, b = c & 1;
+                    const float* gt = reinterpret_cast<const float*>(sptr + e * kCEntry + kCGate);
+                    // (1) v^ = e^{g_last - g} v_new (or v_new), bf16 into TMEM
+                    wait(bar(B_GREADY + e), (c / 3) & 1);
+                    wait(bar(B_M1W), c & 1);
+                    __syncwarp();
+                    tc::tc_fence_after();
+                    const bool fold = gt[kGscal + 1] != 0.f;
+                    {
+                        float x[32];
+                        tc::tmem_ld32(tmem + lane_off + kTD1v + 64 * b + 32 * hh, x);
+                        tc::tmem_wait_ld();
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int e2 = 0; e2 < 16; ++e2) {
-                        const float2 kd = fold ? *reinterpret_cast<const float2*>(gt + kGkdec + 32 * hh + 2 * e2)
-                                               : make_float2(1.f, 1.f);
-                        pk[e2] = tc::pack_bf16(x[2 * e2] * kd.x, x[2 * e2 + 1] * kd.y);
+                        for (int e2 = 0; e2 < 16; ++e2) {
+                            const float2 kd = fold ? *reinterpret_cast<const float2*>(gt + kGkdec + 32 * hh + 2 * e2)
+                                                   : make_float2(1.f, 1.f);
+                            pk[e2] = tc::pack_bf16(x[2 * e2] * kd.x, x[2 * e2 + 1] * kd.y);
+                        }
+                        tc::tmem_st16(tmem + lane_off + kTVN + 16 * hh, pk);
+                        tc::tmem_wait_st();
                     }
-                    tc::tmem_st16(tmem + lane_off + kTVN + 16 * hh, pk);
-                    tc::tmem_wait_st();
+                    tc::tc_fence_before();
+                    tc::named_bar(2, 256);
+                    if (cl) tc::mbar_arrive(bar(B_VREADY));
+                    __syncwarp();
+                    // (2) S += v^^T k done: S is now the state after chunk c
+                    wait(bar(B_M2), c & 1);
+                    __syncwarp();
+                    tc::tc_fence_after();
                 }
-                tc::tc_fence_before();
-                tc::named_bar(2, 256);
-                if (cl) tc::mbar_arrive(bar(B_VREADY));
-                __syncwarp();
-                // (2) S (bf16) for the next chunk's MMAs; q, k of a strong-decay next chunk
-                wait(bar(B_M2), c & 1);
-                __syncwarp();
-                tc::tc_fence_after();
+                // (3) S (bf16) for the next chunk's MMAs; q, k of a strong-decay next chunk
                 float egl_next = 1.f;
                 if (c + 1 < nch) {
                     snapshot();
@@ -836,7 +837,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tc::named_bar(2, 256);
                 if (cl && c + 1 < nch) tc::mbar_arrive(bar(B_SREADY));
                 __syncwarp();
-                // (3) while the next MMAs run: S (fp32) <- e^{g_last} S for the next chunk;
+                // (4) while the next MMAs run: S (fp32) <- e^{g_last} S for the next chunk;
                 // the named barrier after the next v^ orders it before the next S += v^^T k
                 if (GDN && c + 1 < nch) decay(egl_next);
             }
@@ -863,20 +864,49 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (lane == 0) tc::mbar_arrive(bar(B_GREADY + e));
                 __syncwarp();
             }
+        } else if (warp == 15) {
+            // ---- the solve CTA's P^, -w (chain entry c % 3) and T'' (apply entry c % 2),
+            // loaded from its global scratch slot c % 3 once it is stored there and the
+            // entries are free
+            const char* const slot0 = scratch + (size_t)unit * kScratchUnit;
+            int issued = 0;
+            for (int c = 0; c < nch && !dead; ++c) {
+                const int e = c % 3, a = c & 1, sl = c % kSlots;
+                wait.remote(bar(B_STORED + sl), (c / kSlots) & 1);
+                if (c >= 3) wait(bar(B_CFREE + e), (c / 3 - 1) & 1);
+                if (c >= 2) wait(bar(B_AFREE + a), ((c >> 1) - 1) & 1);
+                __syncwarp();
+                if (lane == 0 && !*abort_flag) {
+                    const char* const slot = slot0 + sl * kScratchSlot;
+                    const uint32_t ce = sbase + e * kCEntry, ae = sbase + kARing + a * kAEntry;
+                    tc::fence_proxy_async_global();
+                    tc::mbar_arrive_expect_tx(bar(B_FULLP + e), GDN ? 4 * 8192 : 2 * 8192);
+                    tc::bulk_load(ce + kCP, slot, 8192, bar(B_FULLP + e));
+                    tc::bulk_load(ae + kAT2, slot + 8192, 8192, bar(B_FULLP + e));
+                    if (GDN) tc::bulk_load(ce + kCW, slot + 16384, 16384, bar(B_FULLP + e));
+                    issued = c + 1;
+                }
+                __syncwarp();
+            }
+            // after an abort, let the loads already issued land before the CTA exits
+            if (lane == 0 && *abort_flag)
+                for (int c = max(0, issued - 3); c < issued; ++c) tc::mbar_wait(bar(B_FULLP + c % 3), (c / 3) & 1);
+            __syncwarp();
         } else {
             // ---- the MMA warp: every MMA of the back, in chunk order
-            const bool L = lane == 0;
             for (int c = 0; c < nch && !dead; ++c) {
                 const int e = c % 3, a = c & 1, b = c & 1;
                 const uint32_t ce = sbase + e * kCEntry, ae = sbase + kARing + a * kAEntry;
                 // D1v[b] = u^T = v^T T''^T
                 wait(bar(B_FULLA + a), (c >> 1) & 1);
-                wait.remote(bar(B_FULLP + e), (c / 3) & 1);
+                wait(bar(B_FULLP + e), (c / 3) & 1);
+                if (lane == 0) tc::mbar_arrive_remote_relaxed(peer_bar_f + 8u * (F_ARMED + c % kSlots));  // slot read
+                __syncwarp();
                 if (!*abort_flag) {
                     tc::tc_fence_after();
-                    tc::mma_batch_ss(L, tmem + kTD1v + 64 * b, tc::sdesc(ae + kAV, kBBox, 1024), 128,
-                                     tc::sdesc(ae + kAT2, 16, 1024), 2, kIdWU, 4, false);
-                    tc::mma_commit_p(L, bar(B_AFREE + a));
+                    tc::mma_ss_n<4>(tmem + kTD1v + 64 * b, tc::sdesc(ae + kAV, kBBox, 1024), 128,
+                                    tc::sdesc(ae + kAT2, 16, 1024), 2, kIdWU, false);
+                    tc::commit_e(bar(B_AFREE + a));
                 }
                 // D1v[b] += S (-w)^T once S(c) is in TMEM
                 wait(bar(B_SREADY), c & 1);
@@ -884,31 +914,29 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (!*abort_flag) {
                     tc::tc_fence_after();
                     if (GDN)
-                        tc::mma_batch_ts(L, tmem + kTD1v + 64 * b, tmem + kTS, 8, tc::sdesc(ce + kCW, kBBox, 1024), 128,
-                                         kId1w, 8, true);
-                    tc::mma_commit_p(L, bar(B_M1W));
+                        tc::mma_ts_n<8>(tmem + kTD1v + 64 * b, tmem + kTS, 8, tc::sdesc(ce + kCW, kBBox, 1024), 128,
+                                        kId1w, true);
+                    tc::commit_e(bar(B_M1W));
                 }
                 // D1o[b] = S q^T once the output warps have read D1o[b]
                 if (c >= 2) wait(bar(B_D1OF + b), ((c >> 1) - 1) & 1);
                 if (!*abort_flag) {
                     tc::tc_fence_after();
-                    tc::mma_batch_ts(L, tmem + kTD1o + 64 * b, tmem + kTS, 8, tc::sdesc(ce + kCQ, 16, 1024), 2, kId1q, 4,
-                                     false);
-                    tc::mma_batch_ts(L, tmem + kTD1o + 64 * b, tmem + kTS + 32, 8, tc::sdesc(ce + kCQ + kBBox, 16, 1024), 2,
-                                     kId1q, 4, true);
+                    tc::mma_ts_n<4>(tmem + kTD1o + 64 * b, tmem + kTS, 8, tc::sdesc(ce + kCQ, 16, 1024), 2, kId1q, false);
+                    tc::mma_ts_n<4>(tmem + kTD1o + 64 * b, tmem + kTS + 32, 8, tc::sdesc(ce + kCQ + kBBox, 16, 1024), 2,
+                                    kId1q, true);
                 }
                 // S += v^^T k; D1o[b] += v^^T P^^T
                 wait(bar(B_VREADY), c & 1);
                 if (!*abort_flag) {
                     tc::tc_fence_after();
-                    tc::mma_batch_ts(L, tmem + kTD2, tmem + kTVN, 8, tc::sdesc(ce + kCK, kBBox, 1024), 128, kId2, 4, true);
-                    tc::mma_commit_p(L, bar(B_M2));
-                    tc::mma_batch_ts(L, tmem + kTD1o + 64 * b, tmem + kTVN, 8, tc::sdesc(ce + kCP, 16, 1024), 2, kId3, 4,
-                                     true);
-                    tc::mma_commit_p(L, bar(B_M3 + b));
+                    tc::mma_ts_n<4>(tmem + kTD2, tmem + kTVN, 8, tc::sdesc(ce + kCK, kBBox, 1024), 128, kId2, true);
+                    tc::commit_e(bar(B_M2));
+                    tc::mma_ts_n<4>(tmem + kTD1o + 64 * b, tmem + kTVN, 8, tc::sdesc(ce + kCP, 16, 1024), 2, kId3, true);
+                    tc::commit_e(bar(B_M3 + b));
                 }
             }
-            tc::mma_commit_p(L, bar(B_FIN));
+            tc::commit_e(bar(B_FIN));
         }
     }
 
@@ -925,6 +953,17 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 }
 
 }  // namespace pair
+
+// Workspace of the cluster kernel: the plan, then the per-(sequence, head)
+// global scratch slots at the next 1 KB boundary.
+static size_t pair_scratch_offset(int n_seqs) { return (PlanLayout(n_seqs).end + 1023) & ~(size_t)1023; }
+size_t pair_workspace_bytes(int n_seqs, int H) {
+    return pair_scratch_offset(n_seqs) + (size_t)n_seqs * (size_t)H * pair::kScratchUnit;
+}
+
+bool pair_shape_ok(const PrefillArgs& a) {
+    return a.io == GDN_BF16 && a.dk == 128 && a.dv == 128 && (!a.delta_rule || a.H % 4 == 0);
+}
 
 bool pair_supported(const PrefillArgs& a) {
     auto al = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
@@ -970,7 +1009,8 @@ cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mla, mb, mo, a.h0, (__nv_bfloat16*)a.o, a.h_T, a.ws, a.H);
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mla, mb, mo, a.h0, (__nv_bfloat16*)a.o, a.h_T, a.ws,
+                           a.ws + pair_scratch_offset(a.n_seqs), a.H);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

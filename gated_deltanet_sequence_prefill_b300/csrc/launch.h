@@ -54,7 +54,9 @@ cudaError_t launch_fused(const PrefillArgs& a, cudaStream_t st);
 
 // Fused prefill on a 2-CTA cluster per (sequence, head): solve on one SM,
 // state pass on the other (bf16, dk = dv = 128).
+bool pair_shape_ok(const PrefillArgs& a);  // sizes and dtype only
 bool pair_supported(const PrefillArgs& a);
+size_t pair_workspace_bytes(int n_seqs, int H);  // plan + global scratch
 cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t st);
 
 }  // namespace gdn

@@ -98,11 +98,32 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                  "r"(x), "r"(y), "r"(z), "r"(src)
                  : "memory");
 }
+// Untiled bulk copies between shared and global memory (both addresses
+// 16-byte aligned, size a multiple of 16).  The store joins the thread's bulk
+// group (bulk_commit / bulk_wait*); the load counts its bytes on `bar`.
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     sdst),
+                 "l"(gsrc), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+// Order global-memory accesses of the generic proxy with the async proxy
+// (bulk copies) of this thread, and release / acquire them at GPU scope.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the committed stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Wait until the committed stores are complete.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait1() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -202,6 +223,49 @@ static __device__ __noinline__ void mma_batch_ts(bool leader, uint32_t d, uint32
     for (int k = 0; k < n; ++k)
         mma_bf16_ta_p(leader, d, a0 + k * a_step, b0 + (uint64_t)(k * b_step), idesc, (k > 0) || acc0);
 }
+// Elected-lane forms for a converged warp: every lane executes the
+// instruction, elect.sync picks the one lane that issues it.  Straight-line
+// (unrolled, inlined) sequences of these issue several times faster than a
+// loop or a called helper, which pay for moving the operands into uniform
+// registers on every MMA.  The commit must come from the same elected lane as
+// the MMAs it tracks, so it is issued the same way.
+__device__ __forceinline__ void mma_ss_e(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p, e; .reg .b32 r; setp.ne.b32 p, %4, 0; elect.sync r|e, 0xffffffff;"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p, e; .reg .b32 r; setp.ne.b32 p, %4, 0; elect.sync r|e, 0xffffffff;"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void commit_e(uint32_t bar) {
+    asm volatile(
+        "{ .reg .pred e; .reg .b32 r; elect.sync r|e, 0xffffffff;"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }" ::"r"(bar)
+        : "memory");
+}
+// N K-slices of one MMA shape, unrolled; descriptors advance by a_step /
+// b_step 16-byte units per slice (a TMEM A operand by a_step columns).
+template <int N>
+__device__ __forceinline__ void mma_ss_n(uint32_t d, uint64_t a0, uint32_t a_step, uint64_t b0, uint32_t b_step,
+                                         uint32_t idesc, bool acc0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+        mma_ss_e(d, a0 + (uint64_t)(k * a_step), b0 + (uint64_t)(k * b_step), idesc, (k > 0 || acc0) ? 1u : 0u);
+}
+template <int N>
+__device__ __forceinline__ void mma_ts_n(uint32_t d, uint32_t a0, uint32_t a_step, uint64_t b0, uint32_t b_step,
+                                         uint32_t idesc, bool acc0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+        mma_ts_e(d, a0 + k * a_step, b0 + (uint64_t)(k * b_step), idesc, (k > 0 || acc0) ? 1u : 0u);
+}
 // Arrive on `bar` once every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -277,6 +341,12 @@ __device__ __forceinline__ void cluster_sync() {
 // Arrive on an mbarrier of another CTA of the cluster (release, cluster scope).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+// The same arrive without release semantics: for a signal that orders none of
+// this thread's own memory writes (a release here waits for them to drain).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                  : "memory");
 }
 // 16-byte store into another CTA's shared memory; its completion is counted

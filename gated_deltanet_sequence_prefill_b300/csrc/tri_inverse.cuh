@@ -54,9 +54,9 @@ __device__ __forceinline__ void tri_inverse_64(float* M, float* scratch, int pw,
 
     const int g = lane >> 2, t4 = lane & 3;
     float* scr = scratch + pw * 128;  // 16 x 8, row stride 8
-#pragma unroll
+#pragma unroll 1
     for (int d = 1; d < 4; ++d) {
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 2; ++q) {
             const int tile = pw + 4 * q;
             if (tile < 2 * (4 - d)) {
