@@ -86,6 +86,24 @@ bool use_pair(const PrefillArgs& a) {
     return !(e != nullptr && e[0] == '0');
 }
 
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// Solve CTAs per cluster for the cluster kernel: two (a 3-SM cluster) when
+// every (sequence, head) then still has its cluster at once, else one (more
+// clusters side by side pay off more than a faster solve).
+// GDN_PREFILL_FRONTS=1 or 2 in the environment forces the choice.
+int pair_fronts(const PrefillArgs& a) {
+    const char* e = getenv("GDN_PREFILL_FRONTS");
+    if (e != nullptr && (e[0] == '1' || e[0] == '2')) return e[0] - '0';
+    return 3LL * a.n_seqs * a.H <= (long long)sm_count() ? 2 : 1;
+}
+
 gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
     const bool pair = use_pair(a);
     const bool fused = pair || fused_supported(a);
@@ -95,7 +113,7 @@ gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
     if (s != GDN_OK) return s;
     if (!fused) return run_staged(a, st, nullptr, nullptr, nullptr, nullptr, true);
     cudaError_t e = launch_plan(a.cu_seqlens, a.n_seqs, a.T_total, a.ws, st);
-    if (e == cudaSuccess) e = pair ? launch_pair(a, st) : launch_fused(a, st);
+    if (e == cudaSuccess) e = pair ? launch_pair(a, pair_fronts(a), st) : launch_fused(a, st);
     return cuda_status(e);
 }
 

@@ -205,6 +205,10 @@ __device__ __forceinline__ bool opaque(bool f) {
     asm volatile("" : "+r"(v));
     return v != 0;
 }
+__device__ __forceinline__ int opaque_i(int x) {
+    asm volatile("" : "+r"(x));
+    return x;
+}
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
@@ -263,7 +267,7 @@ __device__ __noinline__ void derive_gates(const float* la_raw, const float* b_ra
     __syncwarp();
 }
 
-template <bool GDN>
+template <bool GDN, int FR>
 __global__ void __launch_bounds__(kThreads, 1)
 pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
@@ -281,8 +285,11 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     // and the loops over chunks they bound, as warp-uniform
     const bool dead = __shfl_sync(0xffffffffu, hdr->status, 0) != GDN_OK;  // uniform across the cluster
 
+    // cluster of FR solve CTAs (ranks 0 .. FR-1; solve CTA r takes the chunks
+    // c = r, r + FR, ...) and one state CTA (rank FR)
     const uint32_t rank = tc::cluster_rank();
-    const bool front = rank == 0;
+    const bool front = rank < (uint32_t)FR;
+    const int fr = opaque_i(front ? (int)rank : 0);
     // the warp index and the TMEM base are broadcast from lane 0 so that the
     // compiler sees them as warp-uniform: role branches then stay in uniform
     // control flow and MMA descriptors are built in uniform registers
@@ -292,12 +299,13 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     PlanLayout L(n_seqs);
     const int* cu = reinterpret_cast<const int*>(ws + L.cu);
     const int* order = reinterpret_cast<const int*>(ws + L.order);
-    const int unit = blockIdx.x >> 1;
+    const int unit = blockIdx.x / (FR + 1);
     const int seq = dead ? 0 : __shfl_sync(0xffffffffu, order[unit / H], 0);
     const int head = unit % H;
     const int start = dead ? 0 : __shfl_sync(0xffffffffu, cu[seq], 0);
     const int len = dead ? 0 : __shfl_sync(0xffffffffu, cu[seq + 1], 0) - start;
     const int nch = (len + kChunk - 1) / kChunk;
+    const int nu = opaque_i(front ? (nch - fr + FR - 1) / FR : 0);  // this solve CTA's chunks
 
     const uint32_t bar_base = sbase + (front ? kFBar : kBBar);
     auto bar = [&](int i) { return bar_base + 8u * (uint32_t)i; };
@@ -334,22 +342,22 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
 
     // peer addresses
-    const uint32_t peer_base = tc::map_to_rank(sbase, 1);           // back smem, seen from the front
-    const uint32_t peer_bar_b = peer_base + kBBar;
-    const uint32_t peer_bar_f = tc::map_to_rank(sbase + kFBar, 0);  // front barriers, seen from the back
+    const uint32_t peer_bar_b = tc::map_to_rank(sbase + kBBar, FR);  // state CTA's barriers
+    const uint32_t peer_bar_f0 = tc::map_to_rank(sbase + kFBar, 0);  // solve CTAs' barriers
+    const uint32_t peer_bar_f1 = tc::map_to_rank(sbase + kFBar, FR - 1);
 
 
     if (front) {
         // ============================================================ FRONT
         if (warp == 0) {
-            // ---- TMA issue only (chunk c in stage c % 3): runs ahead as far as the
-            // ring allows; [k; q] k^T and the gate values are warp 13's
+            // ---- TMA issue only (this CTA's u-th chunk in stage u % 4): runs ahead as
+            // far as the ring allows; [k; q] k^T and the gate values are warp 13's
             int issued = 0;
-            for (int c = 0; c < nch && !dead; ++c) {
-                const int f = c % kFStages, uf = c / kFStages;
+            for (int u = 0; u < nu && !dead; ++u) {
+                const int f = u % kFStages, uf = u / kFStages;
                 const uint32_t st = sbase + f * kFStage;
-                if (c >= kFStages) wait(bar(F_EMPTY + f), (uf - 1) & 1);
-                const int t0 = start + c * kChunk;
+                if (u >= kFStages) wait(bar(F_EMPTY + f), (uf - 1) & 1);
+                const int t0 = start + (fr + FR * u) * kChunk;
                 if (lane == 0 && !*abort_flag) {
                     tc::mbar_arrive_expect_tx(bar(F_FULL + f), 32768 + (GDN ? 2048 : 0));
                     tc::tma_load_3d(st + kFK0, &tm_k, 0, head, t0, bar(F_FULL + f));
@@ -360,9 +368,9 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         tc::tma_load_2d(st + kFGRaw, &tm_la, head & ~3, t0, bar(F_FULL + f));
                         tc::tma_load_2d(st + kFGRaw + 1024, &tm_b, head & ~3, t0, bar(F_FULL + f));
                     }
-                    issued = c + 1;
-                    if (c + 4 < nch) {
-                        const int tp = t0 + 4 * kChunk;
+                    issued = u + 1;
+                    if (u + 4 < nu) {
+                        const int tp = t0 + 4 * FR * kChunk;
                         tc::tma_prefetch_3d(&tm_k, 0, head, tp);
                         tc::tma_prefetch_3d(&tm_k, 64, head, tp);
                         tc::tma_prefetch_3d(&tm_q, 0, head, tp);
@@ -376,11 +384,11 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 __syncwarp();
             }
             if (lane == 0 && *abort_flag)
-                for (int c = max(0, issued - kFStages); c < issued; ++c)
-                    tc::mbar_wait(bar(F_FULL + c % kFStages), (c / kFStages) & 1);
+                for (int u = max(0, issued - kFStages); u < issued; ++u)
+                    tc::mbar_wait(bar(F_FULL + u % kFStages), (u / kFStages) & 1);
             __syncwarp();
         } else if (warp <= 12) {
-            // ---- solve groups: group g takes chunks c with c % 3 == g
+            // ---- solve groups: group g takes this CTA's chunks u with u % 3 == g
             const int grp = (warp - 1) >> 2;  // 0, 1, 2
             const int pw = (warp - 1) & 3;    // warp within the group
             const int nb = 1 + grp;           // named barrier of the group
@@ -388,17 +396,17 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             float* AF = reinterpret_cast<float*>(sptr + kFAF + grp * 64 * kTriLd * 4);
             float* scr = reinterpret_cast<float*>(sptr + kFScr + grp * 4 * 128 * 4);
             const uint32_t pst = sbase + kFPst + grp * 8192;
-            for (int c = grp; c < nch && !dead; c += kFGroups) {
-                const int uf = c / kFGroups;
-                const uint32_t stg = sbase + (c % kFStages) * kFStage;
+            for (int u = grp; u < nu && !dead; u += kFGroups) {
+                const int uf = u / kFGroups;
+                const uint32_t stg = sbase + (u % kFStages) * kFStage;
                 wait(bar(F_GREADY + grp), uf & 1);
                 wait(bar(F_P1D + grp), uf & 1);
                 // P^ staging and AF are rewritten below: the store warp must have read
                 // this group's previous chunk out of them
-                if (c >= kFGroups) wait(bar(F_SFREE + grp), (uf - 1) & 1);
+                if (u >= kFGroups) wait(bar(F_SFREE + grp), (uf - 1) & 1);
                 __syncwarp();
                 tc::tc_fence_after();
-                const float* gt = reinterpret_cast<const float*>(sptr + (c % kFStages) * kFStage + kFGate);
+                const float* gt = reinterpret_cast<const float*>(sptr + (u % kFStages) * kFStage + kFGate);
                 const bool safe = gt[kGscal + 1] != 0.f;
                 const int n = (int)gt[kGscal + 2];
                 const int t = row & 63;
@@ -409,12 +417,15 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 // the same o and h.
                 {
                     const bool is_a = row < 64;
-                    // safe factors: A[t][s] = KK[t][s] beta_t e^{g_t} e^{-g_s}, P^[t][s] = QK[t][s] e^{-g_last}
-                    const float rs = is_a ? gt[kGbb + t] * gt[kGeg + t] : gt[kGscal + 3];
+                    // safe factors: A[t][s] = KK[t][s] beta_t e^{g_t} e^{-g_s} (row t >= n of
+                    // the chunk zeroed; entries on and above the diagonal are never read by the
+                    // inverse, so they are not masked), P^[t][s] = QK[t][s] e^{-g_last} for
+                    // s <= t (rows t >= n produce outputs that are never stored)
+                    const bool tok = t < n;
+                    const float rs = is_a ? (tok ? gt[kGbb + t] * gt[kGeg + t] : 0.f) : gt[kGscal + 3];
                     const float* const en = gt + (is_a ? kGeng : kGone);
                     const float gtt = gt[kGg + t], bsc = is_a ? gt[kGbb + t] : 1.f;
                     const int lim = is_a ? t : t + 1;
-                    const bool tok = t < n;
 #pragma unroll 1
                     for (int part = 0; part < 4; ++part) {
                         float x[16];
@@ -426,11 +437,14 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
                                 for (int q4 = 0; q4 < 4; ++q4) {
                                     const float4 f = *reinterpret_cast<const float4*>(en + s0 + 4 * q4);
-                                    const int s1 = s0 + 4 * q4;
-                                    x[4 * q4 + 0] = (tok && s1 + 0 < lim) ? x[4 * q4 + 0] * f.x * rs : 0.f;
-                                    x[4 * q4 + 1] = (tok && s1 + 1 < lim) ? x[4 * q4 + 1] * f.y * rs : 0.f;
-                                    x[4 * q4 + 2] = (tok && s1 + 2 < lim) ? x[4 * q4 + 2] * f.z * rs : 0.f;
-                                    x[4 * q4 + 3] = (tok && s1 + 3 < lim) ? x[4 * q4 + 3] * f.w * rs : 0.f;
+                                    x[4 * q4 + 0] *= f.x * rs;
+                                    x[4 * q4 + 1] *= f.y * rs;
+                                    x[4 * q4 + 2] *= f.z * rs;
+                                    x[4 * q4 + 3] *= f.w * rs;
+                                }
+                                if (!is_a) {  // warp-uniform: the P^ rows are warps 2, 3 of the group
+#pragma unroll
+                                    for (int e2 = 0; e2 < 16; ++e2) x[e2] = s0 + e2 <= t ? x[e2] : 0.f;
                                 }
                             } else {
 #pragma unroll
@@ -534,11 +548,12 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         } else if (warp == 13) {
             // ---- [k; q] k^T into DP1[c % 3] and the chunk's gate values, as each
             // chunk lands
-            for (int c = 0; c < nch && !dead; ++c) {
-                const int f = c % kFStages, g = c % kFGroups, ug = c / kFGroups;
+            for (int u = 0; u < nu && !dead; ++u) {
+                const int c = fr + FR * u;
+                const int f = u % kFStages, g = u % kFGroups, ug = u / kFGroups;
                 const uint32_t st = sbase + f * kFStage;
-                wait(bar(F_FULL + f), (c / kFStages) & 1);
-                if (c >= kFGroups) wait(bar(F_P1F + g), (ug - 1) & 1);
+                wait(bar(F_FULL + f), (u / kFStages) & 1);
+                if (u >= kFGroups) wait(bar(F_P1F + g), (ug - 1) & 1);
                 __syncwarp();
                 if (!*abort_flag) {
                     tc::tc_fence_after();
@@ -556,14 +571,15 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             tc::commit_e(bar(F_FIN));  // once its last MMA is done
             __syncwarp();
         } else if (warp >= 14) {
-            // ---- store warps (14: even chunks, 15: odd chunks): each chunk's P^, T'' and
+            // ---- store warps (14: even u, 15: odd u): each chunk's P^, T'' and
             // -w go from the group's staging to this unit's global scratch slot c % 6
             // (bulk copies through L2; the state CTA loads them from there) and are
             // announced once written.  A slot is rewritten only after the state CTA has
             // read the chunk it held before.
             char* const slot0 = scratch + (size_t)unit * kScratchUnit;
-            for (int c = warp - 14; c < nch && !dead; c += 2) {
-                const int grp = c % kFGroups, uf = c / kFGroups, sl = c % kSlots;
+            for (int u = warp - 14; u < nu && !dead; u += 2) {
+                const int c = fr + FR * u;
+                const int grp = u % kFGroups, uf = u / kFGroups, sl = c % kSlots;
                 wait(bar(F_STAGED + grp), uf & 1);
                 if (c >= kSlots) wait.remote(bar(F_ARMED + sl), (c / kSlots - 1) & 1);
                 __syncwarp();
@@ -572,13 +588,13 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     if (go) {
                         char* const slot = slot0 + sl * kScratchSlot;
                         tc::bulk_store(slot, sbase + kFPst + grp * 8192, 8192);
-                        tc::bulk_store(slot + 8192, sbase + (c % kFStages) * kFStage + kFT2, 8192);
+                        tc::bulk_store(slot + 8192, sbase + (u % kFStages) * kFStage + kFT2, 8192);
                         if (GDN) tc::bulk_store(slot + 16384, sbase + kFAF + grp * 64 * kTriLd * 4, 16384);
                         tc::bulk_commit();
                         tc::bulk_wait_read0();
                     }
                     tc::mbar_arrive(bar(F_SFREE + grp));  // the staging and the stage may be reused
-                    tc::mbar_arrive(bar(F_EMPTY + c % kFStages));
+                    tc::mbar_arrive(bar(F_EMPTY + u % kFStages));
                     if (go) {  // the slot's writes are done: tell the state CTA
                         tc::bulk_wait0();
                         tc::fence_proxy_async_global();
@@ -900,7 +916,8 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 // D1v[b] = u^T = v^T T''^T
                 wait(bar(B_FULLA + a), (c >> 1) & 1);
                 wait(bar(B_FULLP + e), (c / 3) & 1);
-                if (lane == 0) tc::mbar_arrive_remote_relaxed(peer_bar_f + 8u * (F_ARMED + c % kSlots));  // slot read
+                if (lane == 0)  // slot read: the solve CTA of chunk c may rewrite it
+                    tc::mbar_arrive_remote_relaxed((c % FR == 0 ? peer_bar_f0 : peer_bar_f1) + 8u * (F_ARMED + c % kSlots));
                 __syncwarp();
                 if (!*abort_flag) {
                     tc::tc_fence_after();
@@ -975,11 +992,12 @@ bool pair_supported(const PrefillArgs& a) {
     return al(a.q, 16) && al(a.k, 16) && al(a.v, 16) && tensor_map_encoder() != nullptr;
 }
 
-cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t st) {
+cudaError_t launch_pair(const PrefillArgs& a, int fronts, cudaStream_t st) {
     using namespace pair;
     const long long units = (long long)a.n_seqs * a.H;
     if (units == 0) return cudaSuccess;
-    if (2 * units > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (fronts != 1 && fronts != 2) return cudaErrorInvalidValue;
+    if ((fronts + 1) * units > 0x7fffffffLL) return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv, mla, mb, mo;
     const int64_t T = a.T_total > 0 ? a.T_total : 1;
     const void* base = a.q ? a.q : a.ws;
@@ -994,17 +1012,18 @@ cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t st) {
         mla = mq;
         mb = mq;
     }
-    auto kern = a.delta_rule ? pair_kernel<true> : pair_kernel<false>;
+    auto kern = fronts == 2 ? (a.delta_rule ? pair_kernel<true, 2> : pair_kernel<false, 2>)
+                            : (a.delta_rule ? pair_kernel<true, 1> : pair_kernel<false, 1>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * units), 1, 1);
+    cfg.gridDim = dim3((unsigned)((fronts + 1) * units), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemAlloc;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = fronts + 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

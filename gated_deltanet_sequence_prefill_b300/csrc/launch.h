@@ -57,6 +57,7 @@ cudaError_t launch_fused(const PrefillArgs& a, cudaStream_t st);
 bool pair_shape_ok(const PrefillArgs& a);  // sizes and dtype only
 bool pair_supported(const PrefillArgs& a);
 size_t pair_workspace_bytes(int n_seqs, int H);  // plan + global scratch
-cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t st);
+// fronts: solve CTAs per cluster (1 or 2), next to the one state CTA.
+cudaError_t launch_pair(const PrefillArgs& a, int fronts, cudaStream_t st);
 
 }  // namespace gdn

@@ -28,21 +28,34 @@ __device__ __forceinline__ const float* tri_block_row(const float* M, int t, int
     return jb == ib ? M + t * kTriLd + 16 * ib : M + (16 * jb + a) * kTriLd + 16 * ib;
 }
 
-// On entry M holds A (zero on and above the diagonal); on exit the layout
-// above.  Called by the 128 threads of warps pw = 0..3 (warp index within the
+// TF32 operand of a warp-level MMA: the fp32 bits as they are, of which the
+// MMA uses the tf32 part (no separate rounding step; the result is rounded to
+// bf16 by its users, far coarser than either rounding).
+__device__ __forceinline__ uint32_t tf32_bits(float x) { return __float_as_uint(x); }
+
+// On entry M holds A below the diagonal (entries on and above it are never
+// read); on exit the layout above.  Called by the 128 threads of warps pw = 0..3 (warp index within the
 // group) with named barrier `bar_id`; `scratch` is 4 x 128 floats.
 __device__ __forceinline__ void tri_inverse_64(float* M, float* scratch, int pw, int lane,
                                                int bar_id) {
     {
         float* B = M + (16 * pw) * kTriLd + 16 * pw;
         const int c = lane & 15;
+        // column c by forward substitution, one row of B at a time (four entries
+        // per load; entries on and above the diagonal are never used)
         float y[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = (i == c) ? 1.f : 0.f;
+        for (int rr = 0; rr < 16; ++rr) {
+            float acc = (rr == c) ? 1.f : 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-#pragma unroll
-            for (int rr = i + 1; rr < 16; ++rr) y[rr] = fmaf(-B[rr * kTriLd + i], y[i], y[rr]);
+            for (int i4 = 0; i4 < rr; i4 += 4) {
+                const float4 b = *reinterpret_cast<const float4*>(B + rr * kTriLd + i4);
+                acc = fmaf(-b.x, y[i4], acc);
+                if (i4 + 1 < rr) acc = fmaf(-b.y, y[i4 + 1], acc);
+                if (i4 + 2 < rr) acc = fmaf(-b.z, y[i4 + 2], acc);
+                if (i4 + 3 < rr) acc = fmaf(-b.w, y[i4 + 3], acc);
+            }
+            y[rr] = acc;
         }
         __syncwarp();
         if (lane < 16) {
@@ -66,13 +79,13 @@ __device__ __forceinline__ void tri_inverse_64(float* M, float* scratch, int pw,
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const float* Ar = M + (16 * i + g) * kTriLd + 16 * k + 8 * kk + t4;
-                        uint32_t a[4] = {tc::to_tf32(Ar[0]), tc::to_tf32(Ar[8 * kTriLd]),
-                                         tc::to_tf32(Ar[4]), tc::to_tf32(Ar[8 * kTriLd + 4])};
+                        uint32_t a[4] = {tf32_bits(Ar[0]), tf32_bits(Ar[8 * kTriLd]),
+                                         tf32_bits(Ar[4]), tf32_bits(Ar[8 * kTriLd + 4])};
                         // T_kj rows 8kk + t4 (+4), column n0 + g of block j
                         const float* Br = (k == j)
                                               ? M + (16 * j + 8 * kk + t4) * kTriLd + 16 * j + n0 + g
                                               : M + (16 * j + 8 * kk + t4) * kTriLd + 16 * k + n0 + g;
-                        uint32_t b[2] = {tc::to_tf32(Br[0]), tc::to_tf32(Br[4 * kTriLd])};
+                        uint32_t b[2] = {tf32_bits(Br[0]), tf32_bits(Br[4 * kTriLd])};
                         tc::mma_tf32(c, a, b);
                     }
                 }
@@ -85,10 +98,10 @@ __device__ __forceinline__ void tri_inverse_64(float* M, float* scratch, int pw,
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const float* Tr = M + (16 * i + g) * kTriLd + 16 * i + 8 * kk + t4;
-                    uint32_t a[4] = {tc::to_tf32(Tr[0]), tc::to_tf32(Tr[8 * kTriLd]),
-                                     tc::to_tf32(Tr[4]), tc::to_tf32(Tr[8 * kTriLd + 4])};
-                    uint32_t b[2] = {tc::to_tf32(scr[(8 * kk + t4) * 8 + g]),
-                                     tc::to_tf32(scr[(8 * kk + t4 + 4) * 8 + g])};
+                    uint32_t a[4] = {tf32_bits(Tr[0]), tf32_bits(Tr[8 * kTriLd]),
+                                     tf32_bits(Tr[4]), tf32_bits(Tr[8 * kTriLd + 4])};
+                    uint32_t b[2] = {tf32_bits(scr[(8 * kk + t4) * 8 + g]),
+                                     tf32_bits(scr[(8 * kk + t4 + 4) * 8 + g])};
                     tc::mma_tf32(e, a, b);
                 }
                 __syncwarp();
