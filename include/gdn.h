@@ -96,9 +96,11 @@ GDN_API size_t gdn_chunk_fwd_workspace_size(int64_t T_total, int H, int dk, int 
  * produced for every token).  Chunk size 64; chunks restart at every
  * sequence start and the last chunk of a sequence may be partial.
  * For bf16 with dk = dv = 128 the call runs one fused kernel that puts each
- * (sequence, head) on a 2-SM cluster; GDN_PREFILL_PAIR=0 in the environment
- * selects the kernel with one CTA per (sequence, head, 64-column half of the
- * state) instead (same results up to rounding).
+ * (sequence, head) on a cluster of one or two solve SMs and one state SM (two
+ * when 3 x n_seqs x H <= the SM count; GDN_PREFILL_FRONTS=1 or =2 in the
+ * environment forces it); GDN_PREFILL_PAIR=0 selects the kernel with one CTA
+ * per (sequence, head, 64-column half of the state) instead (same results up
+ * to rounding).
  */
 GDN_API gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
                          const float *log_alpha, const float *beta, const float *h0,

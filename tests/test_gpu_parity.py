@@ -93,7 +93,18 @@ def test_gdn_ragged_varlen(g, dk, dv, dtype, staged):
     assert rel(hT, rh) <= TOL[dtype], rel(hT, rh)
 
 
-KERNELS = [pytest.param("1", id="pair"), pytest.param("0", id="single_sm")]
+# (GDN_PREFILL_PAIR, GDN_PREFILL_FRONTS): the cluster kernel with one or two
+# solve CTAs per cluster, and the single-SM kernel
+KERNELS = [pytest.param(("1", "1"), id="pair_1solve"), pytest.param(("1", "2"), id="pair_2solve"),
+           pytest.param(("0", None), id="single_sm")]
+
+
+def use_kernel(monkeypatch, kernel):
+    monkeypatch.setenv("GDN_PREFILL_PAIR", kernel[0])
+    if kernel[1] is None:
+        monkeypatch.delenv("GDN_PREFILL_FRONTS", raising=False)
+    else:
+        monkeypatch.setenv("GDN_PREFILL_FRONTS", kernel[1])
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -102,7 +113,7 @@ def test_gdn_strong_gates(g, monkeypatch, kernel, scale):
     """Strongly negative log-decays: a chunk's decay range (about 30 at scale
     6, about 200 at scale 40) straddles or passes the limit of the factored
     form, so both decay paths of each fused kernel run."""
-    monkeypatch.setenv("GDN_PREFILL_PAIR", kernel)
+    use_kernel(monkeypatch, kernel)
     inp = gi.gdn_inputs([700, 333, 129], 4, 128, 128, "bf16", h0_std=0.5, seed=5)
     inp["log_alpha"] = inp["log_alpha"] * scale
     o, hT = run_gdn(g, inp)
@@ -117,7 +128,7 @@ def test_fused_kernels(g, monkeypatch, kernel, lengths, h0_std):
     """Each fused kernel, forced through the environment, against the oracle
     on ragged packed sequences (the automatic choice picks the cluster kernel
     for these few units)."""
-    monkeypatch.setenv("GDN_PREFILL_PAIR", kernel)
+    use_kernel(monkeypatch, kernel)
     inp = gi.gdn_inputs(lengths, 4, 128, 128, "bf16", h0_std=h0_std, seed=3)
     o, hT = run_gdn(g, inp)
     ro, rh = ref_gdn(inp)
@@ -183,10 +194,13 @@ def test_gdn_t32768_h16(g):
     check_chains(inp, o, hT, [(0, 0), (0, 5), (0, 11), (0, 15)], TOL["bf16"])
 
 
-def test_pair_kernel_varlen_t131072_h32(g, monkeypatch):
-    """The 2-SM cluster kernel, forced, on the benchmarked packed call (128
-    clusters, more than fit at once): 8 sampled chains against the oracle."""
+@pytest.mark.parametrize("fronts", ["1", "2"])
+def test_pair_kernel_varlen_t131072_h32(g, monkeypatch, fronts):
+    """The cluster kernel with one or two solve CTAs, forced, on the
+    benchmarked packed call (128 clusters, more than fit at once): 8 sampled
+    chains against the oracle."""
     monkeypatch.setenv("GDN_PREFILL_PAIR", "1")
+    monkeypatch.setenv("GDN_PREFILL_FRONTS", fronts)
     lengths = gi.varlen_lengths(131072, 4, 0)
     inp = gi.gdn_inputs(lengths, 32, 128, 128, "bf16", h0_std=0.01, seed=0)
     o, hT = run_gdn(g, inp)
