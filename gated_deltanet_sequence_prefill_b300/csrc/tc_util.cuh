@@ -181,48 +181,6 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// Warp-converged forms: every lane of the warp executes the instruction and
-// only `leader` issues it (a lone diverged issuer pays far more per MMA).
-__device__ __forceinline__ void mma_bf16_p(bool leader, uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{ .reg .pred p, l; setp.ne.b32 p, %4, 0; setp.ne.b32 l, %5, 0;"
-        " @l tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"((uint32_t)leader)
-        : "memory");
-}
-__device__ __forceinline__ void mma_bf16_ta_p(bool leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                              uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{ .reg .pred p, l; setp.ne.b32 p, %4, 0; setp.ne.b32 l, %5, 0;"
-        " @l tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"((uint32_t)leader)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit_p(bool leader, uint32_t bar) {
-    asm volatile(
-        "{ .reg .pred l; setp.ne.b32 l, %1, 0;"
-        " @l tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }" ::"r"(bar),
-        "r"((uint32_t)leader)
-        : "memory");
-}
-// n K-slices of one MMA shape from a single issue site (warp-converged,
-// `leader` issues).  Descriptors advance by a_step / b_step 16-byte units per
-// slice (a TMEM A operand by a_step columns).  Keeping every MMA of a loop on
-// these two sites keeps the issue cost near the tensor pipe's own rate; many
-// distinct inline MMA sites in one loop issue several times slower.
-static __device__ __noinline__ void mma_batch_ss(bool leader, uint32_t d, uint64_t a0, uint32_t a_step, uint64_t b0,
-                                          uint32_t b_step, uint32_t idesc, int n, bool acc0) {
-#pragma unroll 1
-    for (int k = 0; k < n; ++k)
-        mma_bf16_p(leader, d, a0 + (uint64_t)(k * a_step), b0 + (uint64_t)(k * b_step), idesc, (k > 0) || acc0);
-}
-static __device__ __noinline__ void mma_batch_ts(bool leader, uint32_t d, uint32_t a0, uint32_t a_step, uint64_t b0,
-                                          uint32_t b_step, uint32_t idesc, int n, bool acc0) {
-#pragma unroll 1
-    for (int k = 0; k < n; ++k)
-        mma_bf16_ta_p(leader, d, a0 + k * a_step, b0 + (uint64_t)(k * b_step), idesc, (k > 0) || acc0);
-}
 // Elected-lane forms for a converged warp: every lane executes the
 // instruction, elect.sync picks the one lane that issues it.  Straight-line
 // (unrolled, inlined) sequences of these issue several times faster than a
