@@ -742,17 +742,20 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const uint32_t d2 = tmem + lane_off + kTD2 + 64 * hh;
             const uint32_t ts = tmem + lane_off + kTS + 32 * hh;
             // S (bf16) <- S (fp32)
+            // (both halves loaded before one wait: this step is on the state chain's
+            // critical path)
             auto snapshot = [&]() {
-#pragma unroll 1
-                for (int part = 0; part < 2; ++part) {
-                    float d[32];
-                    tc::tmem_ld32(d2 + 32 * part, d);
-                    tc::tmem_wait_ld();
-                    uint32_t pk[16];
+                float d[32], d1[32];
+                tc::tmem_ld32(d2, d);
+                tc::tmem_ld32(d2 + 32, d1);
+                tc::tmem_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-                    for (int e2 = 0; e2 < 16; ++e2) pk[e2] = tc::pack_bf16(d[2 * e2], d[2 * e2 + 1]);
-                    tc::tmem_st16(ts + 16 * part, pk);
-                }
+                for (int e2 = 0; e2 < 16; ++e2) pk[e2] = tc::pack_bf16(d[2 * e2], d[2 * e2 + 1]);
+                tc::tmem_st16(ts, pk);
+#pragma unroll
+                for (int e2 = 0; e2 < 16; ++e2) pk[e2] = tc::pack_bf16(d1[2 * e2], d1[2 * e2 + 1]);
+                tc::tmem_st16(ts + 16, pk);
                 tc::tmem_wait_st();
             };
             // S (fp32) *= f
@@ -814,8 +817,8 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (c >= 0) {
                     const int e = c % 3, b = c & 1;
                     const float* gt = reinterpret_cast<const float*>(sptr + e * kCEntry + kCGate);
-                    // (1) v^ = e^{g_last - g} v_new (or v_new), bf16 into TMEM
-                    wait(bar(B_GREADY + e), (c / 3) & 1);
+                    // (1) v^ = e^{g_last - g} v_new (or v_new), bf16 into TMEM (the chunk's
+                    // gate values were waited for when it was prescaled)
                     wait(bar(B_M1W), c & 1);
                     __syncwarp();
                     tc::tc_fence_after();
@@ -838,17 +841,16 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     tc::named_bar(2, 256);
                     if (cl) tc::mbar_arrive(bar(B_VREADY));
                     __syncwarp();
-                    // (2) S += v^^T k done: S is now the state after chunk c
+                }
+                // (2) q, k of a strong-decay next chunk, while S += v^^T k runs
+                const float egl_next = c + 1 < nch ? prescale(c + 1) : 1.f;
+                if (c >= 0) {  // S is now the state after chunk c
                     wait(bar(B_M2), c & 1);
                     __syncwarp();
                     tc::tc_fence_after();
                 }
-                // (3) S (bf16) for the next chunk's MMAs; q, k of a strong-decay next chunk
-                float egl_next = 1.f;
-                if (c + 1 < nch) {
-                    snapshot();
-                    egl_next = prescale(c + 1);
-                }
+                // (3) S (bf16) for the next chunk's MMAs
+                if (c + 1 < nch) snapshot();
                 tc::tc_fence_before();
                 tc::named_bar(2, 256);
                 if (cl && c + 1 < nch) tc::mbar_arrive(bar(B_SREADY));
