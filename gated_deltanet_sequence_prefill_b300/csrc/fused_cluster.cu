@@ -1,45 +1,51 @@
-// fused_cluster.cu -- chunked GDN / linear-attention prefill on a pair of SMs
-// (a 2-CTA thread-block cluster per (sequence, head)), sm_103a, bf16 I/O,
-// dk = dv = 128, chunk 64.
+// fused_cluster.cu -- chunked GDN / linear-attention prefill on a thread-block
+// cluster per (sequence, head): FR solve CTAs (FR = 1 or 2) and one state CTA,
+// sm_103a, bf16 I/O, dk = dv = 128, chunk 64.
 //
 // The chunk stages of the SparseGDN article ("Чем дорог префилл в Gated Delta
 // Networks…": intra-chunk delta-system solve, sequential pass over chunks,
-// outputs from chunk-start states) are split across the two SMs of the pair
-// so that the long-latency solve never holds the buffers the sequential
-// state pass needs.  The state pass works on the transpose S = h^T (dv x dk),
-// so that S and v_new are tensor-core A operands held in TMEM:
+// outputs from chunk-start states) are split across the SMs of the cluster so
+// that the long-latency solve never holds the buffers the sequential state
+// pass needs.  The state pass works on the transpose S = h^T (dv x dk), so
+// that S and v_new are tensor-core A operands held in TMEM.
 //
-//  front CTA (rank 0): the delta-system solve, up to three chunks ahead
+//  solve CTA r (ranks 0..FR-1): the delta-system solve of chunks r, r+FR, ...
 //    TMA warp   q, k (2 x 64x64 SW128 boxes each) and the gates of the head
-//               into a 3-stage ring; chunk-local cumsum g and decay factors;
-//               [k; q] k^T on tcgen05 (M=128 N=64 K=128) into TMEM
-//    3 solve warpgroups, chunk c on group c % 3 (one per ring stage):
+//               into a 4-stage ring
+//    warp 13    [k; q] k^T on tcgen05 (M=128 N=64 K=128) into TMEM; the
+//               chunk's cumsum g and decay factors
+//    3 solve warpgroups, chunk u on group u % 3:
 //               A = beta KK^T exp(g_i - g_j) (strictly lower),
 //               P^ = QK^T e^{-g_last} (causal; QK^T exp(g_i - g_j) when the
 //                    chunk's decay range is large),
 //               T = (I + A)^-1 (tri_inverse.cuh),
-//               w^T = k^T (T diag(beta e^g))^T on tcgen05,
-//               then -w (as [dk][t]), P^ and T diag(beta) are pushed into the
-//               back CTA's shared memory with st.async
-//  back CTA (rank 1): everything that touches the state
-//    TMA warp   q, k into a 3-entry ring, v and the gates into a 2-entry ring;
-//               the gate factors the back needs
+//               T' = T diag(beta e^g) and T'' = T diag(beta) into the dead q tile,
+//               w^T = k^T T'^T on tcgen05, -w staged as [dk][t]
+//    2 store warps  bulk-copy P^, T'' and -w into the (sequence, head)'s global
+//               scratch slot c % 6 (it stays in L2) and announce it to the state
+//               CTA with a remote mbarrier arrive
+//  state CTA (rank FR): everything that touches the state
+//    TMA warp   q, k into a 3-entry ring, v and the gates into a 2-entry ring
+//    loader     bulk-loads each chunk's P^, T'', -w from its scratch slot
+//    gates      the gate factors the state CTA needs
 //    chain      8 warps, each thread one row j of S and one 64-column half;
 //               S in TMEM twice: fp32 (the accumulator of D2) and bf16 (the
 //               A operand)
-//               D1v  = u^T = v^T (T diag(beta))^T, then += S (-w)^T: v_new^T
+//               D1v  = u^T = v^T T''^T, then += S (-w)^T: v_new^T
 //               D1o  = S q^T
 //               v^ = e^{g_last - g} v_new (bf16, TMEM)
 //               S <- e^{g_last} S (fp32, in place), then S += v^^T k on the
 //               tensor core;  D1o += v^^T P^^T
 //    output     4 warps: o = e^{g} D1o, staged in the dead k tile and written
 //               with a TMA store
-//    MMA warp   issues every MMA of the back, warp-converged (lane 0 issues)
+//    MMA warp   issues every MMA of the state CTA as straight-line elect.sync
+//               sequences
 //
 // HBM sees q, k, v, gates, h0 in and o, h_T out; q and k are read by both
-// CTAs (the second read is an L2 hit).  All waits are bounded; a wait that
-// runs out sets GDN_ERR_TIMEOUT in the workspace status word and both CTAs
-// unwind without skipping any barrier.
+// kinds of CTA (the second read is an L2 hit) and the scratch ring never
+// leaves L2.  All waits are bounded; a wait that runs out sets GDN_ERR_TIMEOUT
+// in the workspace status word and the CTAs unwind without skipping any
+// barrier.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -85,8 +91,8 @@ constexpr uint32_t kFEnd = kFBar + kBarSlots * 8 + 64;
 constexpr uint32_t kBBox = 8192;  // stride between the two 64-column boxes
 constexpr uint32_t kCQ = 0, kCK = 16384, kCW = 32768, kCP = 49152, kCGate = 57344;
 constexpr uint32_t kCEntry = 59392;
-// Apply ring (2 entries, chunk c in entry c % 2): v (two boxes), T'' pushed
-// by the front, the raw log-decay of four heads.
+// Apply ring (2 entries, chunk c in entry c % 2): v (two boxes), T'' loaded
+// from the scratch slot, the raw log-decay of four heads.
 constexpr uint32_t kARing = 3 * kCEntry;
 constexpr uint32_t kAV = 0, kAT2 = 16384, kALa = 24576;
 constexpr uint32_t kAEntry = 25600;
@@ -129,7 +135,7 @@ enum {
 enum {
     B_FULLC = 0,    // [3] q, k landed in the chain entry
     B_FULLA = 3,    // [2] v, log-decay landed in the apply entry
-    B_FULLP = 5,    // [3] -w, P^, T'' pushed by the front (counted on the chain entry)
+    B_FULLP = 5,    // [3] -w, P^, T'' loaded from the scratch slot (counted on the chain entry)
     B_GREADY = 8,   // [3] gate values derived into the chain entry
     B_CFREE = 11,   // [3] chain entry free (o store has read its staging)
     B_AFREE = 14,   // [2] apply entry free (u MMA done)
@@ -608,8 +614,8 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     } else {
         // ============================================================ BACK
         if (warp == 0) {
-            // ---- TMA into both rings and arming of the first pushes (issue only;
-            // warp 14 derives the gate values)
+            // ---- TMA into both rings (issue only; warp 14 derives the gate values,
+            // warp 15 loads the solve CTA's tiles)
             int issued = 0;
             for (int c = 0; c < nch && !dead; ++c) {
                 const int e = c % 3, a = c & 1;
