@@ -177,8 +177,12 @@ def test_linear_b2_t4096_h8(g):
     assert rel(o, qo) <= TOL["bf16"] and rel(hT, qh) <= TOL["bf16"]
 
 
-def test_linear_ragged_with_h0(g):
-    inp = gi.linear_inputs([1, 100, 0, 257], 2, 128, 128, "bf16", h0_std=0.5, seed=4)
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_linear_ragged_with_h0(g, monkeypatch, kernel):
+    """Ragged linear attention with an initial state through each fused kernel
+    (the gate-free instantiation: T is the identity, P^ is the causal q k^T)."""
+    use_kernel(monkeypatch, kernel)
+    inp = gi.linear_inputs([1, 100, 0, 257], 4, 128, 128, "bf16", h0_std=0.5, seed=4)
     d = dev(inp)
     o, hT, ws = g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"])
     assert g.workspace_status(ws) == 0
