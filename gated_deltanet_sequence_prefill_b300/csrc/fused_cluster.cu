@@ -480,12 +480,15 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (gissuer) tc::mbar_arrive(bar(F_P1F + grp));
                 __syncwarp();
                 if (GDN) tri_inverse_64(AF, scr, pw, lane, nb);
-                // T' = T diag(beta e^g) (bf16, K-major) for w^T = k^T T'^T on this SM (rows
-                // 0..63), and T'' = T diag(beta) for the state CTA's u MMA (rows 64..127),
-                // both into the stage's dead q tile, 16 columns at a time.  T is the inverse
-                // (GDN) or the identity.
+                // T' = R T diag(beta e^g) (bf16, K-major) for w^T = k^T T'^T on this SM
+                // (rows 0..63), and T'' = R T diag(beta) for the state CTA's u MMA (rows
+                // 64..127), both into the stage's dead q tile, 16 columns at a time.  T is
+                // the inverse (GDN) or the identity.  R = diag(e^{g_last - g}) when the
+                // decay range is moderate (else I): it makes the state CTA's u - S w^T
+                // come out as v^ = e^{g_last - g} v_new directly.
                 {
                     const float* cs = gt + (row < 64 ? kGbeg : kGbb);
+                    const float rf = safe ? gt[kGkdec + t] : 1.f;
                     const uint32_t dst = stg + (row < 64 ? kFT1 : kFT2);
 #pragma unroll 1
                     for (int jb = 0; jb < 4; ++jb) {
@@ -496,14 +499,14 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                             for (int e4 = 0; e4 < 16; e4 += 4) {
                                 const float4 tv = *reinterpret_cast<const float4*>(Tr + e4);
                                 const float4 sv = *reinterpret_cast<const float4*>(cs + 16 * jb + e4);
-                                v[e4] = tv.x * sv.x;
-                                v[e4 + 1] = tv.y * sv.y;
-                                v[e4 + 2] = tv.z * sv.z;
-                                v[e4 + 3] = tv.w * sv.w;
+                                v[e4] = tv.x * sv.x * rf;
+                                v[e4 + 1] = tv.y * sv.y * rf;
+                                v[e4 + 2] = tv.z * sv.z * rf;
+                                v[e4 + 3] = tv.w * sv.w * rf;
                             }
                         } else {
 #pragma unroll
-                            for (int e4 = 0; e4 < 16; ++e4) v[e4] = (!GDN && 16 * jb + e4 == t) ? cs[t] : 0.f;
+                            for (int e4 = 0; e4 < 16; ++e4) v[e4] = (!GDN && 16 * jb + e4 == t) ? cs[t] * rf : 0.f;
                         }
 #pragma unroll
                         for (int h2 = 0; h2 < 2; ++h2)
@@ -821,25 +824,19 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             // (One copy of each step keeps this warp's instruction footprint small.)
             for (int c = -1; c < nch && !dead; ++c) {
                 if (c >= 0) {
-                    const int e = c % 3, b = c & 1;
-                    const float* gt = reinterpret_cast<const float*>(sptr + e * kCEntry + kCGate);
-                    // (1) v^ = e^{g_last - g} v_new (or v_new), bf16 into TMEM (the chunk's
-                    // gate values were waited for when it was prescaled)
+                    const int b = c & 1;
+                    // (1) v^ = e^{g_last - g} v_new (or v_new) to bf16 in TMEM: the solve CTA
+                    // folded the factor into the rows of T' and T'', so D1v already holds it
                     wait(bar(B_M1W), c & 1);
                     __syncwarp();
                     tc::tc_fence_after();
-                    const bool fold = gt[kGscal + 1] != 0.f;
                     {
                         float x[32];
                         tc::tmem_ld32(tmem + lane_off + kTD1v + 64 * b + 32 * hh, x);
                         tc::tmem_wait_ld();
                         uint32_t pk[16];
 #pragma unroll
-                        for (int e2 = 0; e2 < 16; ++e2) {
-                            const float2 kd = fold ? *reinterpret_cast<const float2*>(gt + kGkdec + 32 * hh + 2 * e2)
-                                                   : make_float2(1.f, 1.f);
-                            pk[e2] = tc::pack_bf16(x[2 * e2] * kd.x, x[2 * e2 + 1] * kd.y);
-                        }
+                        for (int e2 = 0; e2 < 16; ++e2) pk[e2] = tc::pack_bf16(x[2 * e2], x[2 * e2 + 1]);
                         tc::tmem_st16(tmem + lane_off + kTVN + 16 * hh, pk);
                         tc::tmem_wait_st();
                     }
