@@ -23,6 +23,7 @@ Arrays are token-major: q,k [T,H,dk], v [T,H,dv], log_alpha/beta [T,H],
 h0/hT [N,H,dk,dv] with h = S^T.  Inputs may be numpy arrays or CPU torch
 tensors of any float dtype; they are upcast to float64 exactly.
 """
+import contextlib
 import ctypes
 import os
 
@@ -33,27 +34,43 @@ from . import build as _build
 _LIB = None
 
 
+def _load(path):
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    ip = ctypes.POINTER(ctypes.c_int64)
+    lib.oracle_recurrent.argtypes = [dp, dp, dp, dp, dp, dp, ip, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     dp, dp, ctypes.c_int]
+    lib.oracle_recurrent.restype = ctypes.c_int
+    lib.oracle_chunked.argtypes = [dp, dp, dp, dp, dp, dp, ip, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+    lib.oracle_chunked.restype = ctypes.c_int
+    lib.oracle_num_chunks.argtypes = [ip, ctypes.c_int, ctypes.c_int]
+    lib.oracle_num_chunks.restype = ctypes.c_int64
+    lib.oracle_num_threads.argtypes = [ctypes.c_int]
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
 def _lib():
     global _LIB
     if _LIB is None:
-        path = _build.build()
-        lib = ctypes.CDLL(path)
-        dp = ctypes.POINTER(ctypes.c_double)
-        ip = ctypes.POINTER(ctypes.c_int64)
-        lib.oracle_recurrent.argtypes = [dp, dp, dp, dp, dp, dp, ip, ctypes.c_int,
-                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                         dp, dp, ctypes.c_int]
-        lib.oracle_recurrent.restype = ctypes.c_int
-        lib.oracle_chunked.argtypes = [dp, dp, dp, dp, dp, dp, ip, ctypes.c_int,
-                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                       ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
-        lib.oracle_chunked.restype = ctypes.c_int
-        lib.oracle_num_chunks.argtypes = [ip, ctypes.c_int, ctypes.c_int]
-        lib.oracle_num_chunks.restype = ctypes.c_int64
-        lib.oracle_num_threads.argtypes = [ctypes.c_int]
-        lib.oracle_num_threads.restype = ctypes.c_int
-        _LIB = lib
+        _LIB = _load(_build.build())
     return _LIB
+
+
+@contextlib.contextmanager
+def using_library(path):
+    """Run the oracle from another build of its source while the context is
+    open (the pins' planted-mistake tests load a deliberately broken copy)."""
+    global _LIB
+    saved = _LIB
+    _LIB = _load(path)
+    try:
+        yield
+    finally:
+        _LIB = saved
 
 
 def _f64(x):

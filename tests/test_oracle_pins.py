@@ -260,3 +260,66 @@ def test_oracle_rejects_bad_seqlens():
     q, k, v, la, b, s0, cu = _rand_case(rng, [4, 4], 1, 2, 2)
     with pytest.raises(ValueError):
         oracle.gdn(q, k, v, la, b, s0, np.array([0, 5, 3, 8]))
+
+
+# --- the pins have teeth: planted mistakes in a private copy of the oracle ---
+#
+# Each entry is a plausible slip in the oracle's arithmetic (a dropped factor, a
+# wrong sign, a wrong operand or index, a transposed read-back, a mask off by
+# one, a decay taken the wrong way).  It is made in a copy of gdn_oracle.c
+# compiled beside the test; the pins above, run against that copy, must reject
+# every one of them.  The oracle itself is not changed.
+
+MUTATIONS = {
+    "delta term without the decay": ("x -= b * (a * Sk[j]) * kt[i];", "x -= b * Sk[j] * kt[i];"),
+    "delta term with the wrong sign": ("x -= b * (a * Sk[j]) * kt[i];", "x += b * (a * Sk[j]) * kt[i];"),
+    "write term without beta": ("x += b * vt[j] * kt[i];", "x += vt[j] * kt[i];"),
+    "output read with k instead of q": ("acc += S[(size_t)j * dk + i] * qt[i];", "acc += S[(size_t)j * dk + i] * kt[i];"),
+    "decay with the wrong sign": ("exp(log_alpha[row])", "exp(-log_alpha[row])"),
+    "final state read back transposed": ("= S[(size_t)j * dk + i];", "= S[(size_t)(i % dv) * dk + (j % dk)];"),
+    "chunk: decay factor reversed in A": ("bi * exp(g[i] - g[j]) * kk;", "bi * exp(g[j] - g[i]) * kk;"),
+    "chunk: A including the diagonal": ("for (int j = 0; j < i; ++j) {\n                        double kk",
+                                        "for (int j = 0; j <= i; ++j) {\n                        double kk"),
+    "chunk: u without beta": ("acc += Tm[(size_t)i * C + j] * bj * v[ROW(j) * dv + y];",
+                              "acc += Tm[(size_t)i * C + j] * v[ROW(j) * dv + y];"),
+    "chunk: intra-chunk mask missing the diagonal": ("for (int j = 0; j <= i; ++j) {\n                        double qk",
+                                                     "for (int j = 0; j < i; ++j) {\n                        double qk"),
+    "chunk: state carried without the decay": ("double acc = exp(gl) * h[(size_t)x * dv + y];",
+                                               "double acc = h[(size_t)x * dv + y];"),
+}
+
+PINS = [
+    ("hand cases", lambda: test_hand_cases()),
+    ("overwrite invariant", lambda: test_delta_rule_overwrite_invariant(16, 16)),
+    ("chunked = recurrent", lambda: test_chunked_equals_recurrent(16, True)),
+    ("chunked = recurrent, no delta", lambda: test_chunked_equals_recurrent(4, False)),
+    ("linear = quadratic form", lambda: test_linear_matches_quadratic_form([7, 0, 33], 5, 3)),
+    ("beta = 0 closed form", lambda: test_beta_zero_closed_form()),
+    ("decay without delta closed form", lambda: test_decay_without_delta_closed_form()),
+    ("transition-matrix product", lambda: test_transition_matrix_product()),
+    ("WY intermediates", lambda: test_wy_intermediates_solve_the_delta_system()),
+]
+
+
+@pytest.mark.parametrize("name", list(MUTATIONS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    import subprocess
+
+    old, new = MUTATIONS[name]
+    src_path = os.path.join(os.path.dirname(oracle.__file__), "gdn_oracle.c")
+    with open(src_path) as f:
+        src = f.read()
+    assert src.count(old) == 1, "mutation site not unique: " + name
+    mutant = tmp_path / "gdn_oracle_mutant.c"
+    mutant.write_text(src.replace(old, new))
+    lib = tmp_path / "liboracle_mutant.so"
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", str(lib), str(mutant), "-lm"],
+                   check=True)
+    caught = []
+    with oracle.using_library(str(lib)):
+        for pin, check in PINS:
+            try:
+                check()
+            except Exception:  # an assertion, or a NaN the comparison trips over
+                caught.append(pin)
+    assert caught, "no pin rejects the planted mistake: " + name
