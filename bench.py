@@ -223,6 +223,23 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x, dist=None, device=None):
+    """The slowest rank's figure.  Every rank runs the same per-GPU workload
+    (weak scaling, no collective on the data path), so the job takes as long as
+    its slowest rank; with one process this is x itself."""
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, ms_per_step):
+    """Whole-job throughput: the tokens all ranks processed over the slowest
+    rank's time."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import gated_deltanet_sequence_prefill_b300 as g
@@ -277,11 +294,8 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError("device status %d" % status)
 
-    ms = torch.tensor([total_ms / args.steps], device="cuda")
-    if dist is not None:
-        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
-    ms_per_step = float(ms.item())
-    value = world * T / (ms_per_step / 1e3)
+    ms_per_step = max_over_ranks(total_ms / args.steps, dist, "cuda")
+    value = job_tokens_per_s(world, T, ms_per_step)
 
     # end to end through the same public call, from and to pinned host memory
     host = {k: v.pin_memory() for k, v in inp.items()}
@@ -307,10 +321,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_call()
     e1.record(stream)
     barrier()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1) / e2e_steps], device="cuda")
-    if dist is not None:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_value = world * T / (float(e2e_ms.item()) / 1e3)
+    e2e_value = job_tokens_per_s(world, T, max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, "cuda"))
 
     if rank == 0:
         pk = peaks()
