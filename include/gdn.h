@@ -80,9 +80,13 @@ GDN_API const char *gdn_version(void);
 
 /*
  * Workspace bytes needed by gdn_chunk_fwd for these sizes (0 on bad sizes).
- * The bf16 path with dk = dv = 128 keeps every intermediate on-chip and needs
- * only a small scheduling area; other combinations run the staged path and
- * need gdn_staged_workspace_size() bytes.
+ * The bf16 path with dk = dv = 128 keeps every intermediate on-chip or in L2:
+ * it needs a small scheduling area plus 192 KB per (sequence, head) through
+ * which the solve SM of each cluster hands its per-chunk tiles to the state
+ * SM (n_seqs * H * 196608 bytes, rounded up to a 1 KB boundary after the
+ * scheduling area); other combinations run the staged path and need
+ * gdn_staged_workspace_size() bytes.  The same holds for
+ * linear_attn_fwd_workspace_size().
  */
 GDN_API size_t gdn_chunk_fwd_workspace_size(int64_t T_total, int H, int dk, int dv, int n_seqs,
                                     gdn_dtype io_dtype);
