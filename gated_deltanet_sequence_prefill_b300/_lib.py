@@ -4,21 +4,23 @@ Every step of the computation runs in the library's CUDA kernels; this module
 checks tensor placement/dtype/contiguity, allocates outputs and workspaces
 with PyTorch (the caller may pass its own), and forwards raw device pointers
 and the current CUDA stream to the C entry points declared in include/gdn.h.
-If the library is missing, importing this module raises: there is no
-fallback implementation.
+If the library is missing or older than its sources, importing this module
+compiles it first (build.py, nvcc for sm_103a); if that fails, the import
+raises: there is no fallback implementation.
 """
 import ctypes
 import os
 
 import torch
 
-_HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgdn_b300.so")
+from . import build as _build
 
-if not os.path.exists(LIB_PATH):
-    raise ImportError(
-        "libgdn_b300.so is not built (%s); run gated_deltanet_sequence_prefill_b300/build.py "
-        "or __graft_entry__.build()" % LIB_PATH)
+LIB_PATH = _build.LIB
+
+try:
+    _build.build()
+except Exception as e:  # no nvcc, or a compile error: no library, no package
+    raise ImportError("libgdn_b300.so could not be built (%s): %s" % (LIB_PATH, e)) from e
 
 lib = ctypes.CDLL(LIB_PATH)
 

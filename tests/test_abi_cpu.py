@@ -13,8 +13,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def g():
-    from gated_deltanet_sequence_prefill_b300 import build as b
-    b.build()
+    # importing the package compiles the library first when it is missing or stale
     import gated_deltanet_sequence_prefill_b300 as pkg
     return pkg
 
