@@ -1,6 +1,7 @@
 // static_scratch.cu -- gdn_chunk_fwd_staged_static: the staged prefill with
 // its scratch in one fixed device array, for callers that cannot allocate
 // device memory (see gdn.h for the contract).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -14,25 +15,70 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_scratch[GDN_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 256;
-void* g_scratch_addr[kMaxDevices];
+
+// Device address of the array, per device, together with the identity of the
+// context it was looked up in.  A device reset (cudaDeviceReset) destroys the
+// primary context and the library's module with it; the next context loads
+// the module again, possibly at another address, and has a new context id,
+// so the address is looked up again.
+struct ScratchSlot {
+    bool valid;
+    unsigned long long ctx_id;
+    void* addr;
+};
+ScratchSlot g_slots[kMaxDevices];
 std::mutex g_scratch_mu;
 
-// Device address of the array on the current device, looked up once per
-// device.  In host code the array's name is only a host-side stand-in, so
-// kernels must be given this address, never the name.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (false if there is none
+// or the driver cannot tell).
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the array in the current device's context.  In host code
+// the array's name is only a host-side stand-in, so kernels must be given
+// this address, never the name.  The lookup (cudaGetSymbolAddress, with the
+// device current) runs once per device and context; later calls reuse it.
 cudaError_t scratch_address(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchSlot& slot = g_slots[dev];
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    if (!slot.valid || !have_id || slot.ctx_id != id) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        e = cudaGetSymbolAddress(&p, g_static_scratch);  // also creates the context if needed
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+        const bool known = current_context_id(&id);
+        slot.valid = known;  // without a context id, look it up on every call
+        slot.ctx_id = id;
+        slot.addr = p;
+        *out = p;
+        return cudaSuccess;
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return cudaSuccess;
 }
 
