@@ -51,6 +51,10 @@ lib.gdn_recurrent_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _fp, _vp, _i, _i, _i
 lib.gdn_recurrent_step.restype = _i
 lib.gdn_workspace_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
 lib.gdn_workspace_status.restype = _i
+lib.gdn_workspace_timeout_site.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
+lib.gdn_workspace_timeout_site.restype = _i
+lib.gdn_set_wait_limit.argtypes = [_i]
+lib.gdn_set_wait_limit.restype = _i
 
 CHUNK = 64
 
@@ -240,3 +244,19 @@ def workspace_status(workspace, stream=None):
     _check(lib.gdn_workspace_status(_ptr(workspace), _stream(workspace, stream), ctypes.byref(st)),
            "gdn_workspace_status")
     return st.value
+
+
+def workspace_timeout_site(workspace, stream=None):
+    """Synchronise the stream and read which barrier the call's first timed-out
+    wait gave up on (0: none)."""
+    site = ctypes.c_int(0)
+    _check(lib.gdn_workspace_timeout_site(_ptr(workspace), _stream(workspace, stream),
+                                          ctypes.byref(site)), "gdn_workspace_timeout_site")
+    return site.value
+
+
+def set_wait_limit(polls):
+    """Polls a bounded device wait makes before it reports GDN_ERR_TIMEOUT, for
+    calls launched from now on (process-wide); negative restores the default.
+    Returns the previous bound."""
+    return int(lib.gdn_set_wait_limit(int(polls)))

@@ -4,6 +4,8 @@
 #include <stdlib.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "gdn.h"
 #include "launch.h"
@@ -11,6 +13,10 @@
 using namespace gdn;
 
 namespace {
+
+// Polls per bounded device wait, for the calls launched from now on.
+constexpr int kDefaultWaitLimit = 1 << 22;
+std::atomic<int> g_wait_limit{kDefaultWaitLimit};
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool head_ok(int d) { return d == 64 || d == 128; }
@@ -58,7 +64,7 @@ gdn_status run_staged(const PrefillArgs& a, cudaStream_t st, float* g_out, float
     if (A_out) b.A = A_out;
     if (w_out) b.w = w_out;
     if (u_out) b.u = u_out;
-    cudaError_t e = launch_plan(a.cu_seqlens, a.n_seqs, a.T_total, a.ws, st);
+    cudaError_t e = launch_plan(a.cu_seqlens, a.n_seqs, a.T_total, g_wait_limit.load(), a.ws, st);
     if (e == cudaSuccess && a.delta_rule && a.T_total > 0) e = launch_kkt(a, b, st);
     if (e == cudaSuccess && a.delta_rule && a.T_total > 0) e = launch_wy(a, b, st);
     if (e == cudaSuccess && state_pass) e = launch_state_ffma(a, b, st);
@@ -112,7 +118,7 @@ gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
     gdn_status s = check_prefill(a, ws_bytes, need, true);
     if (s != GDN_OK) return s;
     if (!fused) return run_staged(a, st, nullptr, nullptr, nullptr, nullptr, true);
-    cudaError_t e = launch_plan(a.cu_seqlens, a.n_seqs, a.T_total, a.ws, st);
+    cudaError_t e = launch_plan(a.cu_seqlens, a.n_seqs, a.T_total, g_wait_limit.load(), a.ws, st);
     if (e == cudaSuccess) e = pair ? launch_pair(a, pair_fronts(a), st) : launch_fused(a, st);
     return cuda_status(e);
 }
@@ -137,7 +143,20 @@ const char* gdn_status_string(int status) {
     }
 }
 
-const char* gdn_version(void) { return "gdn_b300 0.1 sm_103a"; }
+const char* gdn_version(void) { return "gdn_b300 0.2 sm_103a"; }
+
+int gdn_set_wait_limit(int polls) {
+    return g_wait_limit.exchange(polls < 0 ? kDefaultWaitLimit : polls);
+}
+
+gdn_status gdn_workspace_timeout_site(const void* workspace, void* stream, int* site) {
+    if (!workspace || !site) return GDN_ERR_NULL;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(site, (const char*)workspace + offsetof(WsHeader, timeout_site), sizeof(int),
+                       cudaMemcpyDeviceToHost);
+    return cuda_status(e);
+}
 
 size_t gdn_staged_workspace_size(int64_t T, int H, int dk, int dv, int n_seqs, gdn_dtype io) {
     if (!sizes_ok(T, H, dk, dv, n_seqs) || (io != GDN_BF16 && io != GDN_FP32)) return 0;

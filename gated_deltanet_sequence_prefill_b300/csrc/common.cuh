@@ -19,7 +19,9 @@ struct WsHeader {
     int n_seqs;
     int total_chunks;  // sum over sequences of ceil(L_s / 64)
     int max_len;       // longest sequence
-    int pad[59];
+    int timeout_site;  // first barrier a timed-out wait gave up on (0: none)
+    int wait_limit;    // polls a bounded device wait makes before it gives up
+    int pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -175,7 +175,7 @@ constexpr uint32_t kId3 = tc::idesc_bf16(128, 64, false, false);   // A = v^T (T
 __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_flag, int site) {
     WsHeader* h = reinterpret_cast<WsHeader*>(ws);
     atomicExch(&h->status, GDN_ERR_TIMEOUT);
-    atomicCAS(&h->pad[0], 0, site);
+    atomicCAS(&h->timeout_site, 0, site);
     *abort_flag = 1;
 }
 
@@ -184,9 +184,9 @@ __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_fla
 // wait is one out-of-line function: inlined at every call site its loop and
 // timeout path made up a large share of the kernel's instruction footprint.
 static __device__ __noinline__ bool wait_bar(volatile int* abort_flag, char* ws, uint32_t bar, uint32_t parity,
-                                             int site, bool cluster_scope) {
+                                             int site, bool cluster_scope, int limit) {
     if (*abort_flag) return false;
-    if (cluster_scope ? tc::mbar_wait_cluster(bar, parity) : tc::mbar_wait(bar, parity)) return true;
+    if (cluster_scope ? tc::mbar_wait_cluster(bar, parity, limit) : tc::mbar_wait(bar, parity, limit)) return true;
     report_timeout(ws, abort_flag, site);
     return false;
 }
@@ -195,11 +195,12 @@ struct Waiter {
     char* ws;
     uint32_t bar_base;
     int site_base;
+    int limit;  // polls per wait (the call's bound, from the workspace header)
     __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
-        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), false);
+        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), false, limit);
     }
     __device__ __forceinline__ bool remote(uint32_t bar, uint32_t parity) const {
-        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), true);
+        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), true, limit);
     }
 };
 
@@ -317,7 +318,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     auto bar = [&](int i) { return bar_base + 8u * (uint32_t)i; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + (front ? kFBar : kBBar) + kBarSlots * 8);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (front ? kFBar : kBBar) + kBarSlots * 8 + 8);
-    const Waiter wait{abort_flag, ws, bar_base, front ? 1000 : 2000};
+    const Waiter wait{abort_flag, ws, bar_base, front ? 1000 : 2000, __shfl_sync(0xffffffffu, hdr->wait_limit, 0)};
 
     if (tid == 0) {
         *abort_flag = 0;

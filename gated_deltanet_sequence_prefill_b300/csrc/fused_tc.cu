@@ -113,6 +113,7 @@ constexpr uint32_t kId3 = tc::idesc_bf16(128, 64, false, true);
 __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_flag) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     atomicExch(&hdr->status, GDN_ERR_TIMEOUT);
+    atomicCAS(&hdr->timeout_site, 0, 3000);  // this kernel records no barrier index
     *abort_flag = 1;
 }
 
@@ -121,17 +122,19 @@ __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_fla
 // abort (work is skipped, barriers are not), so an abort cannot deadlock.
 // The wait is one out-of-line function: inlined at every call site its loop
 // and timeout path made up a large share of the kernel's instruction footprint.
-static __device__ __noinline__ bool wait_bar(volatile int* abort_flag, char* ws, uint32_t bar, uint32_t parity) {
+static __device__ __noinline__ bool wait_bar(volatile int* abort_flag, char* ws, uint32_t bar, uint32_t parity,
+                                             int limit) {
     if (*abort_flag) return false;
-    if (tc::mbar_wait(bar, parity)) return true;
+    if (tc::mbar_wait(bar, parity, limit)) return true;
     report_timeout(ws, abort_flag);
     return false;
 }
 struct Waiter {
     volatile int* abort_flag;
     char* ws;
+    int limit;  // polls per wait (the call's bound, from the workspace header)
     __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
-        return wait_bar(abort_flag, ws, bar, parity);
+        return wait_bar(abort_flag, ws, bar, parity, limit);
     }
 };
 
@@ -207,7 +210,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + kOffMisc);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + kOffMisc + 8);
-    const Waiter wait{abort_flag, ws};
+    const Waiter wait{abort_flag, ws, __shfl_sync(0xffffffffu, hdr->wait_limit, 0)};
 
     if (tid == 0) {
         *abort_flag = 0;

@@ -39,7 +39,10 @@ struct StagedBuffers {
 size_t staged_intermediate_bytes(int64_t T, int H, int dk, int dv, int n_seqs);
 StagedBuffers staged_buffers(char* ws, int64_t T, int H, int dk, int dv, int n_seqs);
 
-cudaError_t launch_plan(const int32_t* cu, int n_seqs, int64_t T_total, void* ws, cudaStream_t st);
+// wait_limit: polls a bounded device wait of the call's kernels makes before
+// it reports GDN_ERR_TIMEOUT (recorded in the workspace header).
+cudaError_t launch_plan(const int32_t* cu, int n_seqs, int64_t T_total, int wait_limit, void* ws,
+                        cudaStream_t st);
 cudaError_t launch_kkt(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
 cudaError_t launch_wy(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
 cudaError_t launch_state_ffma(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);

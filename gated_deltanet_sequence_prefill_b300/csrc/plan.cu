@@ -11,7 +11,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kOrderQuadraticMax = 4096;  // above this, keep the natural order
 
 __global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs, long long T_total, char* ws) {
+plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs, long long T_total, int wait_limit, char* ws) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     PlanLayout L(n_seqs);
     int* cu = reinterpret_cast<int*>(ws + L.cu);
@@ -39,6 +39,8 @@ plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs, long long T_total, ch
         if (tid == 0) {
             hdr->status = GDN_ERR_SEQLENS;
             hdr->counter = 0;
+            hdr->timeout_site = 0;
+            hdr->wait_limit = wait_limit;
             hdr->n_seqs = n_seqs;
             hdr->total_chunks = 0;
             hdr->max_len = 0;
@@ -81,15 +83,17 @@ plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs, long long T_total, ch
     if (tid == 0) {
         hdr->status = GDN_OK;
         hdr->counter = 0;
-        hdr->pad[0] = 0;
+        hdr->timeout_site = 0;
+        hdr->wait_limit = wait_limit;
         hdr->n_seqs = n_seqs;
         hdr->total_chunks = s_carry;
         hdr->max_len = s_maxlen;
     }
 }
 
-cudaError_t launch_plan(const int32_t* cu, int n_seqs, int64_t T_total, void* ws, cudaStream_t st) {
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(cu, n_seqs, (long long)T_total, (char*)ws);
+cudaError_t launch_plan(const int32_t* cu, int n_seqs, int64_t T_total, int wait_limit, void* ws,
+                        cudaStream_t st) {
+    plan_kernel<<<1, kPlanThreads, 0, st>>>(cu, n_seqs, (long long)T_total, wait_limit, (char*)ws);
     return cudaGetLastError();
 }
 

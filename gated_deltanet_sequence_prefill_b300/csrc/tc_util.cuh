@@ -48,14 +48,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false when the bound ran out (the caller reports GDN_ERR_TIMEOUT).
+// Bounded wait for the phase with the given parity to complete: at most
+// `limit` polls (none when limit <= 0).  Returns false when the bound ran out
+// (the caller reports GDN_ERR_TIMEOUT).  kWaitLimit is the default bound; the
+// waits that drain copies already issued always use it.
 constexpr int kWaitLimit = 1 << 22;
 // (the polling loops are kept rolled: unrolled, each copy cost kilobytes of
 // instruction footprint)
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int limit = kWaitLimit) {
 #pragma unroll 1
-    for (int i = 0; i < kWaitLimit; ++i)
+    for (int i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
@@ -348,9 +350,9 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int limit = kWaitLimit) {
 #pragma unroll 1
-    for (int i = 0; i < kWaitLimit; ++i)
+    for (int i = 0; i < limit; ++i)
         if (mbar_try_wait_cluster(bar, parity)) return true;
     return false;
 }

@@ -185,8 +185,9 @@ GDN_API gdn_status gdn_chunk_prepare(const void *k, const void *v, const float *
  *  - Returns GDN_ERR_WORKSPACE, launching nothing, when the problem needs
  *    more scratch than that (gdn_staged_workspace_size(...) bytes).
  *  - The first call on each device looks up the array's device address
- *    (with that device current); make that first call before any stream
- *    capture.
+ *    (with that device current), and so does the first call after a
+ *    cudaDeviceReset (which recreates the context and the array); make that
+ *    first call before any stream capture.
  *  - Every call shares the one array, which keeps the last call's contents;
  *    the call re-initialises what it reads before reading it.  Calls that
  *    overlap on the GPU (two streams, two threads) race on the array.
@@ -207,6 +208,26 @@ GDN_API gdn_status gdn_chunk_fwd_staged_static(const void *q, const void *k, con
  * by one of the calls above into *status (GDN_OK or a negative gdn_status).
  */
 GDN_API gdn_status gdn_workspace_status(const void *workspace, void *stream, int *status);
+
+/*
+ * Failure detection (no paper counterpart).  Every wait inside the fused
+ * prefill kernels (one SM waiting for another's copy, MMA or hand-off) is
+ * bounded: after `polls` unsuccessful polls of its barrier it gives up, the
+ * call's status word becomes GDN_ERR_TIMEOUT, and every CTA of the call
+ * skips its remaining work (still completing the copies it already issued
+ * and releasing its tensor memory) and exits, leaving the context usable.
+ *  - gdn_set_wait_limit(polls) sets the bound for calls launched afterwards,
+ *    process-wide, and returns the previous one.  The default is 4194304
+ *    (1 << 22); polls < 0 restores it; polls = 0 makes every bounded wait
+ *    give up at once (used by the tests to exercise the timeout path).  The
+ *    outputs of a call that timed out are unspecified.
+ *  - gdn_workspace_timeout_site() waits for `stream`, then reads which
+ *    barrier the first timed-out wait of the call gave up on (0: none;
+ *    1000 + index on a solve CTA, 2000 + index on a state CTA of the cluster
+ *    kernel, 3000 in the single-SM kernel), for diagnosis.
+ */
+GDN_API int gdn_set_wait_limit(int polls);
+GDN_API gdn_status gdn_workspace_timeout_site(const void *workspace, void *stream, int *site);
 
 #ifdef __cplusplus
 }

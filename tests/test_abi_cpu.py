@@ -113,3 +113,12 @@ def test_product_path_does_not_import_the_oracle():
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 assert not pat.search(open(os.path.join(dirpath, f)).read()), f
+
+
+def test_wait_limit_setter(g):
+    # the bound is host state only: set, read back through the next set, restore
+    default = g.set_wait_limit(0)
+    assert default == 1 << 22
+    assert g.set_wait_limit(12345) == 0
+    assert g.set_wait_limit(-1) == 12345
+    assert g.set_wait_limit(-1) == default

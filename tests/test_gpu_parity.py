@@ -60,8 +60,24 @@ def ref_gdn(inp, chains=None):
     return out
 
 
+def ref_heads(inp, chains):
+    """Oracle on the sampled (seq, head) chains, one call per sequence so that
+    its threads run the sampled heads of that sequence in parallel."""
+    cu = inp["cu_seqlens"].tolist()
+    out = {}
+    for s in sorted({c[0] for c in chains}):
+        hs = [h for (s2, h) in chains if s2 == s]
+        a, e = cu[s], cu[s + 1]
+        h0 = None if inp["h0"] is None else inp["h0"][s:s + 1, hs]
+        o, hT = oracle.gdn(inp["q"][a:e, hs], inp["k"][a:e, hs], inp["v"][a:e, hs],
+                           inp["log_alpha"][a:e, hs], inp["beta"][a:e, hs], h0)
+        for i, h in enumerate(hs):
+            out[(s, h)] = (o[:, i], hT[0, i])
+    return out
+
+
 def check_chains(inp, o, hT, chains, tol):
-    ref = ref_gdn(inp, chains)
+    ref = ref_heads(inp, chains)
     cu = inp["cu_seqlens"].tolist()
     o_got = np.concatenate([o[cu[s]:cu[s + 1], h].double().cpu().numpy() for s, h in chains])
     o_ref = np.concatenate([ref[c][0] for c in chains])
@@ -224,13 +240,48 @@ def test_gdn_varlen_t131072_h32(g):
                  TOL["bf16"])
 
 
-def test_staged_matches_fused_call_t32768(g):
-    """The staged three-kernel path and gdn_chunk_fwd agree on a full-size input."""
+@pytest.mark.parametrize("staged", [False, True])
+def test_fused_and_staged_t32768_against_oracle(g, staged):
+    """gdn_chunk_fwd and the staged three-kernel path, each against the oracle
+    on a full-size two-sequence input (sampled chains, every token of each)."""
     inp = gi.gdn_inputs([20000, 12768], 16, 128, 128, "bf16", h0_std=0.01, seed=5)
-    o1, h1 = run_gdn(g, inp)
-    o2, h2 = run_gdn(g, inp, staged=True)
-    assert rel(o1, o2.double().cpu().numpy()) <= TOL["bf16"]
-    assert rel(h1, h2.double().cpu().numpy()) <= TOL["bf16"]
+    o, hT = run_gdn(g, inp, staged=staged)
+    check_chains(inp, o, hT, [(0, 0), (0, 9), (0, 15), (1, 3), (1, 12)], TOL["bf16"])
+
+
+def test_gdn_single_sequence_t131072_h32(g):
+    """The hardest chain: one 131072-token sequence, H = 32 (the automatic
+    choice runs the cluster kernel with two solve CTAs per cluster at full
+    length).  Oracle on sampled heads, every token of each, and h_T."""
+    inp = gi.gdn_inputs([131072], 32, 128, 128, "bf16", h0_std=0.01, seed=0)
+    o, hT = run_gdn(g, inp)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+    check_chains(inp, o, hT, [(0, 0), (0, 13), (0, 22), (0, 31)], TOL["bf16"])
+
+
+# ------------------------------------------------------------------ failure detection
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_forced_wait_timeout_then_recovery(g, monkeypatch, kernel):
+    """With the wait bound at 0 every bounded device wait gives up at once:
+    the call must end (no hang), report GDN_ERR_TIMEOUT and the barrier it
+    gave up on in the workspace, and leave the context usable; a normal call
+    on the same workspace right after matches the oracle."""
+    use_kernel(monkeypatch, kernel)
+    inp = gi.gdn_inputs([300, 77, 129], 4, 128, 128, "bf16", h0_std=0.01, seed=17)
+    d = dev(inp)
+    args = [d[k] for k in ("q", "k", "v", "log_alpha", "beta", "h0", "cu_seqlens")]
+    old = g.set_wait_limit(0)
+    try:
+        _, _, ws = g.gdn_chunk_fwd(*args)
+        assert g.workspace_status(ws) == -9  # GDN_ERR_TIMEOUT
+        assert g.workspace_timeout_site(ws) != 0
+    finally:
+        assert g.set_wait_limit(old) == 0
+    o, hT, ws2 = g.gdn_chunk_fwd(*args, workspace=ws)
+    assert ws2 is ws and g.workspace_status(ws) == 0 and g.workspace_timeout_site(ws) == 0
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
 
 
 # ------------------------------------------------------------------ decode
