@@ -46,6 +46,11 @@ def _load(path):
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
     lib.oracle_chunked.restype = ctypes.c_int
+    lib.oracle_chunked_band.argtypes = [dp, dp, dp, dp, dp, dp, ip, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp, dp, dp,
+                                        ctypes.c_int]
+    lib.oracle_chunked_band.restype = ctypes.c_int
     lib.oracle_num_chunks.argtypes = [ip, ctypes.c_int, ctypes.c_int]
     lib.oracle_num_chunks.restype = ctypes.c_int64
     lib.oracle_num_threads.argtypes = [ctypes.c_int]
@@ -149,9 +154,12 @@ def num_chunks(cu_seqlens, chunk):
 
 
 def chunked(q, k, v, log_alpha=None, beta=None, h0=None, cu_seqlens=None, chunk=64,
-            delta_rule=True, intermediates=False, threads=0):
+            delta_rule=True, intermediates=False, threads=0, band=0):
     """Chunk-wise evaluation.  Returns (o, hT) or, with intermediates=True,
-    (o, hT, dict(A, Tm, w, u, g)) where A/Tm are [n_chunks, H, C, C]."""
+    (o, hT, dict(A, Tm, w, u, g)) where A/Tm are [n_chunks, H, C, C].
+    band > 0: the block-adjacent solver (Tm kept on the diagonal blocks of
+    `band` tokens and the blocks right below them; SparseGDN article,
+    "Двухуровневая разреженность SparseGDN…")."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     la, b, h0 = _f64(log_alpha), _f64(beta), _f64(h0)
     T, H, dk = q.shape
@@ -172,10 +180,16 @@ def chunked(q, k, v, log_alpha=None, beta=None, h0=None, cu_seqlens=None, chunk=
         u = np.zeros((T, H, dv))
         g = np.zeros((T, H))
         inter = dict(A=A, Tm=Tm, w=w, u=u, g=g)
-    rc = _lib().oracle_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(h0),
-                               _ptr(cu, ctypes.c_int64), N, H, dk, dv, int(chunk),
-                               int(bool(delta_rule)), _ptr(o), _ptr(hT), _ptr(A), _ptr(Tm),
-                               _ptr(w), _ptr(u), _ptr(g), int(threads))
+    if band:
+        rc = _lib().oracle_chunked_band(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(h0),
+                                        _ptr(cu, ctypes.c_int64), N, H, dk, dv, int(chunk),
+                                        int(bool(delta_rule)), int(band), _ptr(o), _ptr(hT),
+                                        _ptr(A), _ptr(Tm), _ptr(w), _ptr(u), _ptr(g), int(threads))
+    else:
+        rc = _lib().oracle_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(h0),
+                                   _ptr(cu, ctypes.c_int64), N, H, dk, dv, int(chunk),
+                                   int(bool(delta_rule)), _ptr(o), _ptr(hT), _ptr(A), _ptr(Tm),
+                                   _ptr(w), _ptr(u), _ptr(g), int(threads))
     _check(rc)
     if intermediates:
         return o, hT, inter

@@ -173,14 +173,22 @@ int64_t oracle_num_chunks(const int64_t *cu, int n_seqs, int C)
  * number n (chunks numbered sequence by sequence):
  *   A_out, Tm_out : [n][H][C][C]   (rows past a partial chunk's end are 0 / identity)
  *   w_out         : [t][H][dk],  u_out : [t][H][dv],  g_out : [t][H]
+ *
+ * band > 0 selects the block-adjacent solver of the SparseGDN article
+ * ("Двухуровневая разреженность SparseGDN…", first observation: the solver
+ * restricts the delta system to links between neighbouring blocks, a fixed,
+ * input-independent approximation).  Read here as: Tm is kept on the
+ * diagonal blocks of `band` tokens and on the blocks directly below them,
+ * both exactly as the full inverse has them, and is zero on blocks two or
+ * more apart.  band = 0 is the exact solve.
  */
-int oracle_chunked(const double *q, const double *k, const double *v,
-                   const double *log_alpha, const double *beta,
-                   const double *h0, const int64_t *cu, int n_seqs,
-                   int H, int dk, int dv, int C, int delta_rule,
-                   double *o, double *hT,
-                   double *A_out, double *Tm_out, double *w_out, double *u_out,
-                   double *g_out, int n_threads)
+static int chunked_impl(const double *q, const double *k, const double *v,
+                        const double *log_alpha, const double *beta,
+                        const double *h0, const int64_t *cu, int n_seqs,
+                        int H, int dk, int dv, int C, int delta_rule, int band,
+                        double *o, double *hT,
+                        double *A_out, double *Tm_out, double *w_out, double *u_out,
+                        double *g_out, int n_threads)
 {
     if (!q || !k || !v || !o || H <= 0 || dk <= 0 || dv <= 0 || C <= 0)
         return ORACLE_ERR_ARGS;
@@ -247,6 +255,12 @@ int oracle_chunked(const double *q, const double *k, const double *v,
                     Tm[(size_t)i * C + col] = x;
                 }
             }
+            /* block-adjacent solver: drop the blocks of Tm two or more blocks below
+               the diagonal */
+            if (band > 0)
+                for (int i = 0; i < C; ++i)
+                    for (int col = 0; col < C; ++col)
+                        if (i / band - col / band >= 2) Tm[(size_t)i * C + col] = 0.0;
             /* w = Tm (b e^g K), u = Tm (b V) */
             for (int i = 0; i < n; ++i) {
                 for (int x = 0; x < dk; ++x) {
@@ -313,4 +327,29 @@ int oracle_chunked(const double *q, const double *k, const double *v,
     }
     free(chunk0);
     return status;
+}
+
+int oracle_chunked(const double *q, const double *k, const double *v,
+                   const double *log_alpha, const double *beta,
+                   const double *h0, const int64_t *cu, int n_seqs,
+                   int H, int dk, int dv, int C, int delta_rule,
+                   double *o, double *hT,
+                   double *A_out, double *Tm_out, double *w_out, double *u_out,
+                   double *g_out, int n_threads)
+{
+    return chunked_impl(q, k, v, log_alpha, beta, h0, cu, n_seqs, H, dk, dv, C, delta_rule, 0,
+                        o, hT, A_out, Tm_out, w_out, u_out, g_out, n_threads);
+}
+
+int oracle_chunked_band(const double *q, const double *k, const double *v,
+                        const double *log_alpha, const double *beta,
+                        const double *h0, const int64_t *cu, int n_seqs,
+                        int H, int dk, int dv, int C, int delta_rule, int band,
+                        double *o, double *hT,
+                        double *A_out, double *Tm_out, double *w_out, double *u_out,
+                        double *g_out, int n_threads)
+{
+    if (band <= 0) return ORACLE_ERR_ARGS;
+    return chunked_impl(q, k, v, log_alpha, beta, h0, cu, n_seqs, H, dk, dv, C, delta_rule, band,
+                        o, hT, A_out, Tm_out, w_out, u_out, g_out, n_threads);
 }

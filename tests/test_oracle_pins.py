@@ -244,6 +244,65 @@ def test_wy_intermediates_solve_the_delta_system():
                 assert abs(A[i, j] - expect) < 1e-13
 
 
+# --- block-adjacent solver (SparseGDN article, first observation) -----------
+
+@pytest.mark.parametrize("band", [32, 64, 128])
+def test_block_adjacent_is_exact_when_two_blocks_cover_the_chunk(band):
+    """With blocks of half a chunk or more no block is two blocks below
+    another, so the banded solve is the exact one."""
+    rng = np.random.default_rng(21)
+    q, k, v, la, b, s0, cu = _rand_case(rng, [150, 64, 5], 2, 8, 6)
+    oe, he = oracle.chunked(q, k, v, la, b, s0, cu, chunk=64)
+    ob, hb = oracle.chunked(q, k, v, la, b, s0, cu, chunk=64, band=band)
+    assert _rel(ob, oe) < 1e-13 and _rel(hb, he) < 1e-13
+
+
+def test_block_adjacent_is_exact_for_keys_orthogonal_across_blocks():
+    """Keys of different 16-token blocks on disjoint coordinates: A has no
+    links between blocks, the inverse is block-diagonal, and dropping the
+    far blocks changes nothing (while it does change a generic input)."""
+    rng = np.random.default_rng(22)
+    T, H, dk, dv = 128, 2, 8, 5
+    q, k, v, la, b, s0, cu = _rand_case(rng, [T], H, dk, dv, unit_k=False)
+    for t in range(T):
+        blk = (t % 64) // 16
+        mask = np.zeros(dk)
+        mask[2 * blk:2 * blk + 2] = 1.0
+        k[t] *= mask
+    oe, he = oracle.chunked(q, k, v, la, b, s0, cu, chunk=64)
+    ob, hb = oracle.chunked(q, k, v, la, b, s0, cu, chunk=64, band=16)
+    assert _rel(ob, oe) < 1e-13 and _rel(hb, he) < 1e-13
+    q, k, v, la, b, s0, cu = _rand_case(rng, [T], H, dk, dv, unit_k=False)
+    oe, _ = oracle.chunked(q, k, v, la, b, s0, cu, chunk=64)
+    ob, _ = oracle.chunked(q, k, v, la, b, s0, cu, chunk=64, band=16)
+    assert _rel(ob, oe) > 1e-6
+
+
+def test_block_adjacent_keeps_exactly_the_two_diagonals_of_blocks():
+    """The banded Tm is the exact inverse with the blocks two or more below
+    the diagonal set to zero, and w, u are that Tm applied to b e^g K and
+    b V: blocks one below the diagonal are kept, farther ones dropped."""
+    rng = np.random.default_rng(23)
+    q, k, v, la, b, s0, cu = _rand_case(rng, [64, 40], 1, 6, 4, unit_k=False)
+    _, _, ex = oracle.chunked(q, k, v, la, b, s0, cu, chunk=64, intermediates=True)
+    _, _, bd = oracle.chunked(q, k, v, la, b, s0, cu, chunk=64, intermediates=True, band=16)
+    blk = np.arange(64) // 16
+    far = (blk[:, None] - blk[None, :]) >= 2
+    for c in range(ex["Tm"].shape[0]):
+        Te, Tb = ex["Tm"][c, 0], bd["Tm"][c, 0]
+        np.testing.assert_array_equal(Tb[far], 0.0)
+        np.testing.assert_array_equal(Tb[~far], Te[~far])
+        assert np.any(Te[(blk[:, None] - blk[None, :]) == 1] != 0.0)
+    for s in range(2):
+        a, e = int(cu[s]), int(cu[s + 1])
+        n = e - a
+        Tb = bd["Tm"][s, 0][:n, :n]
+        g = np.cumsum(la[a:e, 0])
+        np.testing.assert_allclose(bd["w"][a:e, 0], Tb @ (b[a:e, 0, None] * np.exp(g)[:, None] * k[a:e, 0]),
+                                   rtol=0, atol=1e-12)
+        np.testing.assert_allclose(bd["u"][a:e, 0], Tb @ (b[a:e, 0, None] * v[a:e, 0]), rtol=0, atol=1e-12)
+
+
 def test_decode_step_equals_one_prefill_token():
     rng = np.random.default_rng(12)
     B, H, dk, dv = 3, 2, 5, 4
@@ -286,6 +345,9 @@ MUTATIONS = {
                                                      "for (int j = 0; j < i; ++j) {\n                        double qk"),
     "chunk: state carried without the decay": ("double acc = exp(gl) * h[(size_t)x * dv + y];",
                                                "double acc = h[(size_t)x * dv + y];"),
+    "band: the blocks right below the diagonal dropped too": ("if (i / band - col / band >= 2)",
+                                                             "if (i / band - col / band >= 1)"),
+    "band: no block dropped": ("if (i / band - col / band >= 2)", "if (i / band - col / band >= 4)"),
 }
 
 PINS = [
@@ -298,6 +360,8 @@ PINS = [
     ("decay without delta closed form", lambda: test_decay_without_delta_closed_form()),
     ("transition-matrix product", lambda: test_transition_matrix_product()),
     ("WY intermediates", lambda: test_wy_intermediates_solve_the_delta_system()),
+    ("banded solve keeps two block diagonals", lambda: test_block_adjacent_keeps_exactly_the_two_diagonals_of_blocks()),
+    ("banded solve exact for orthogonal blocks", lambda: test_block_adjacent_is_exact_for_keys_orthogonal_across_blocks()),
 ]
 
 
