@@ -7,7 +7,8 @@ larger than L2 (4.35 GB), so no L2 flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --workload {gdn_t32768_h16, gdn_t131072_h32_single, gdn_t65536_h8, linear_b2_t4096_h8,
-                              decode_b128_h32}     (the other workloads, one GPU)
+                              decode_b128_h32, gdn_varlen_t131072_h32_block_adjacent}
+                                                   (the other workloads, one GPU)
 
 One JSON line is printed by rank 0.  Under torchrun each rank runs the same
 per-GPU workload on its own GPU (weak scaling, no collective on the data
@@ -414,25 +415,31 @@ def run_workload(args):
         elif name == "gdn_t16384_h4":  # the same length with few units
             lengths, Hh, kind = [16384], 4, "gdn"
             inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
+        elif name == "gdn_varlen_t131072_h32_block_adjacent":  # the headline with the approximate solver
+            lengths, Hh, kind = LENGTHS, H, "gdn_block_adjacent"
+            inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
         else:
             raise SystemExit("unknown workload " + name)
         d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
         Tt, nn = sum(lengths), len(lengths)
         o = torch.empty(Tt, Hh, D, dtype=torch.bfloat16, device="cuda")
         hT = torch.empty(nn, Hh, D, D, dtype=torch.float32, device="cuda")
-        wsz = g.chunk_fwd_workspace_size(Tt, Hh, D, D, nn, delta_rule=(kind == "gdn"))
+        gdn_kind = kind.startswith("gdn")
+        wsz = g.chunk_fwd_workspace_size(Tt, Hh, D, D, nn, delta_rule=gdn_kind)
         ws = torch.empty(max(wsz, 256), dtype=torch.uint8, device="cuda")
-        if kind == "gdn":
+        if gdn_kind:
+            band = kind == "gdn_block_adjacent"
+
             def run():
                 g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["h0"],
-                                d["cu_seqlens"], o=o, h_T=hT, workspace=ws)
+                                d["cu_seqlens"], o=o, h_T=hT, workspace=ws, block_adjacent=band)
         else:
             def run():
                 g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"], o=o, h_T=hT,
                                   workspace=ws)
         units, unit = Tt, "tokens/s"
-        bytes_per_call = 4 * Tt * Hh * D * 2 + (2 * Tt * Hh * 4 if kind == "gdn" else 0) + \
-            (2 if kind == "gdn" else 1) * nn * Hh * D * D * 4
+        bytes_per_call = 4 * Tt * Hh * D * 2 + (2 * Tt * Hh * 4 if gdn_kind else 0) + \
+            (2 if gdn_kind else 1) * nn * Hh * D * D * 4
         launches = 2
         cfg = {"workload": name, "T": Tt, "H": Hh, "dk": D, "dv": D, "seq_lens": lengths,
                "chunk": 64, "path": kernel_name(True, nn * Hh), "l2": ("L2 flushed (256 MB write) between timed calls"
@@ -453,6 +460,12 @@ def run_workload(args):
             times.append(a.elapsed_time(b))
     ms = statistics.median(times)
     achieved = bytes_per_call / (ms / 1e3) / 1e9
+    if name.endswith("_block_adjacent"):
+        # how far the approximate solve lands from the exact one on these inputs
+        o_exact, h_exact, _ = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                              d["h0"], d["cu_seqlens"])
+        rel = lambda x, y: float((x.double() - y.double()).abs().max() / y.double().abs().max())
+        cfg["rel_dev_from_exact_solve"] = {"o": rel(o, o_exact), "h_T": rel(hT, h_exact)}
     line = {"metric": name + " throughput", "value": units / (ms / 1e3), "unit": unit, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "dtype": "bf16", "data": "synthetic (seeded)", "config": cfg,

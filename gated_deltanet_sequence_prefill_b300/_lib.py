@@ -40,6 +40,8 @@ for _n in ("gdn_chunk_fwd_workspace_size", "linear_attn_fwd_workspace_size", "gd
     getattr(lib, _n).restype = _sz
 lib.gdn_chunk_fwd.argtypes = _PREFILL
 lib.gdn_chunk_fwd.restype = _i
+lib.gdn_chunk_fwd_block_adjacent.argtypes = _PREFILL
+lib.gdn_chunk_fwd_block_adjacent.restype = _i
 lib.linear_attn_fwd.argtypes = [_vp, _vp, _vp, _fp, _ip, _i, _i64, _i, _i, _i, _i, _vp, _fp, _vp, _sz, _vp]
 lib.linear_attn_fwd.restype = _i
 lib.gdn_chunk_fwd_staged.argtypes = _PREFILL[:13] + [_i] + _PREFILL[13:]
@@ -157,16 +159,18 @@ def _check_inputs(q, k, v, log_alpha, beta, h0, cu_seqlens):
 
 
 def gdn_chunk_fwd(q, k, v, log_alpha, beta, h0=None, cu_seqlens=None, *, o=None, h_T=None,
-                  workspace=None, output_final_state=True, stream=None):
-    """GDN prefill through the C ABI; returns (o, h_T, workspace)."""
+                  workspace=None, output_final_state=True, stream=None, block_adjacent=False):
+    """GDN prefill through the C ABI; returns (o, h_T, workspace).
+    block_adjacent=True calls gdn_chunk_fwd_block_adjacent (the approximate
+    block-adjacent intra-chunk solver) instead."""
     _check_inputs(q, k, v, log_alpha, beta, h0, cu_seqlens)
     T, H, dk, dv, n = _prefill_shapes(q, k, v, cu_seqlens)
     o, h_T = _outputs(q, v, n, H, dk, dv, o, h_T, output_final_state)
     ws = _alloc_ws(lib.gdn_chunk_fwd_workspace_size(T, H, dk, dv, n, _io(q)), q.device, workspace)
-    rc = lib.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0),
-                           _ptr(cu_seqlens), n, T, H, dk, dv, _io(q), _ptr(o), _ptr(h_T),
-                           _ptr(ws), ws.numel(), _stream(q, stream))
-    _check(rc, "gdn_chunk_fwd")
+    f = lib.gdn_chunk_fwd_block_adjacent if block_adjacent else lib.gdn_chunk_fwd
+    rc = f(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(h0), _ptr(cu_seqlens), n,
+           T, H, dk, dv, _io(q), _ptr(o), _ptr(h_T), _ptr(ws), ws.numel(), _stream(q, stream))
+    _check(rc, "gdn_chunk_fwd_block_adjacent" if block_adjacent else "gdn_chunk_fwd")
     return o, h_T, ws
 
 

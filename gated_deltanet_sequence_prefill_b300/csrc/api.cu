@@ -79,6 +79,7 @@ PrefillArgs make_args(const void* q, const void* k, const void* v, const float* 
     a.q = q; a.k = k; a.v = v; a.log_alpha = la; a.beta = beta; a.h0 = h0;
     a.cu_seqlens = cu; a.n_seqs = n_seqs; a.T_total = T; a.H = H; a.dk = dk; a.dv = dv;
     a.io = io; a.delta_rule = delta; a.o = o; a.h_T = h_T; a.ws = (char*)ws;
+    a.max_block_dist = 3;
     return a;
 }
 
@@ -187,6 +188,18 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          float* h_T, void* workspace, size_t ws_bytes, void* stream) {
     PrefillArgs a = make_args(q, k, v, log_alpha, beta, h0, cu_seqlens, n_seqs, T_total, H, dk, dv,
                               io_dtype, true, o, h_T, workspace);
+    return prefill(a, ws_bytes, (cudaStream_t)stream);
+}
+
+gdn_status gdn_chunk_fwd_block_adjacent(const void* q, const void* k, const void* v,
+                                        const float* log_alpha, const float* beta, const float* h0,
+                                        const int32_t* cu_seqlens, int n_seqs, int64_t T_total,
+                                        int H, int dk, int dv, gdn_dtype io_dtype, void* o,
+                                        float* h_T, void* workspace, size_t ws_bytes,
+                                        void* stream) {
+    PrefillArgs a = make_args(q, k, v, log_alpha, beta, h0, cu_seqlens, n_seqs, T_total, H, dk, dv,
+                              io_dtype, true, o, h_T, workspace);
+    a.max_block_dist = 1;
     return prefill(a, ws_bytes, (cudaStream_t)stream);
 }
 

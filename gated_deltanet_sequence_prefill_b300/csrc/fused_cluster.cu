@@ -183,9 +183,15 @@ __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_fla
 // keeps executing the same sequence of named barriers after an abort.  The
 // wait is one out-of-line function: inlined at every call site its loop and
 // timeout path made up a large share of the kernel's instruction footprint.
+// abort_flag[0] is the CTA's abort flag and abort_flag[1] the call's bound on
+// polls per wait after the first (both in shared memory, so no call site
+// carries the bound; it is read only when the first poll finds the phase
+// incomplete).
 static __device__ __noinline__ bool wait_bar(volatile int* abort_flag, char* ws, uint32_t bar, uint32_t parity,
-                                             int site, bool cluster_scope, int limit) {
+                                             int site, bool cluster_scope) {
     if (*abort_flag) return false;
+    if (cluster_scope ? tc::mbar_try_wait_cluster(bar, parity) : tc::mbar_try_wait(bar, parity)) return true;
+    const int limit = abort_flag[1];
     if (cluster_scope ? tc::mbar_wait_cluster(bar, parity, limit) : tc::mbar_wait(bar, parity, limit)) return true;
     report_timeout(ws, abort_flag, site);
     return false;
@@ -195,12 +201,11 @@ struct Waiter {
     char* ws;
     uint32_t bar_base;
     int site_base;
-    int limit;  // polls per wait (the call's bound, from the workspace header)
     __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
-        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), false, limit);
+        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), false);
     }
     __device__ __forceinline__ bool remote(uint32_t bar, uint32_t parity) const {
-        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), true, limit);
+        return wait_bar(abort_flag, ws, bar, parity, site_base + (int)((bar - bar_base) >> 3), true);
     }
 };
 
@@ -274,7 +279,9 @@ __device__ __noinline__ void derive_gates(const float* la_raw, const float* b_ra
     __syncwarp();
 }
 
-template <bool GDN, int FR>
+// MAXD: farthest 16-token block below the diagonal at which the inverse of
+// the delta system is formed (3: exact; 1: the block-adjacent solver).
+template <bool GDN, int FR, int MAXD>
 __global__ void __launch_bounds__(kThreads, 1)
 pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
@@ -318,10 +325,11 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     auto bar = [&](int i) { return bar_base + 8u * (uint32_t)i; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + (front ? kFBar : kBBar) + kBarSlots * 8);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (front ? kFBar : kBBar) + kBarSlots * 8 + 8);
-    const Waiter wait{abort_flag, ws, bar_base, front ? 1000 : 2000, __shfl_sync(0xffffffffu, hdr->wait_limit, 0)};
+    const Waiter wait{abort_flag, ws, bar_base, front ? 1000 : 2000};
 
     if (tid == 0) {
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        abort_flag[1] = hdr->wait_limit;
 #pragma unroll 1
         for (int b = 0; b < (front ? (int)F_COUNT : (int)B_COUNT); ++b)
             tc::mbar_init(bar(b), (front && b == F_FIN) ? 4 : 1);
@@ -480,7 +488,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tc::named_bar(nb, 128);  // DP1[group] read, A and P^ rows stored
                 if (gissuer) tc::mbar_arrive(bar(F_P1F + grp));
                 __syncwarp();
-                if (GDN) tri_inverse_64(AF, scr, pw, lane, nb);
+                if (GDN) tri_inverse_64(AF, scr, pw, lane, nb, MAXD);
                 // T' = R T diag(beta e^g) (bf16, K-major) for w^T = k^T T'^T on this SM
                 // (rows 0..63), and T'' = R T diag(beta) for the state CTA's u MMA (rows
                 // 64..127), both into the stage's dead q tile, 16 columns at a time.  T is
@@ -494,7 +502,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll 1
                     for (int jb = 0; jb < 4; ++jb) {
                         float v[16];
-                        if (GDN && jb <= (t >> 4)) {
+                        if (GDN && jb <= (t >> 4) && (t >> 4) - jb <= MAXD) {
                             const float* Tr = tri_block_row(AF, t, jb);
 #pragma unroll
                             for (int e4 = 0; e4 < 16; e4 += 4) {
@@ -1018,8 +1026,11 @@ cudaError_t launch_pair(const PrefillArgs& a, int fronts, cudaStream_t st) {
         mla = mq;
         mb = mq;
     }
-    auto kern = fronts == 2 ? (a.delta_rule ? pair_kernel<true, 2> : pair_kernel<false, 2>)
-                            : (a.delta_rule ? pair_kernel<true, 1> : pair_kernel<false, 1>);
+    const bool band = a.delta_rule && a.max_block_dist == 1;
+    auto kern = fronts == 2 ? (band ? pair_kernel<true, 2, 1>
+                                    : a.delta_rule ? pair_kernel<true, 2, 3> : pair_kernel<false, 2, 3>)
+                            : (band ? pair_kernel<true, 1, 1>
+                                    : a.delta_rule ? pair_kernel<true, 1, 3> : pair_kernel<false, 1, 3>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -122,9 +122,13 @@ __device__ __forceinline__ void report_timeout(char* ws, volatile int* abort_fla
 // abort (work is skipped, barriers are not), so an abort cannot deadlock.
 // The wait is one out-of-line function: inlined at every call site its loop
 // and timeout path made up a large share of the kernel's instruction footprint.
-static __device__ __noinline__ bool wait_bar(volatile int* abort_flag, char* ws, uint32_t bar, uint32_t parity,
-                                             int limit) {
+// abort_flag[0] is the CTA's abort flag, abort_flag[1] the call's bound on
+// polls per wait after the first (both in shared memory; the bound is read
+// only when the first poll finds the phase incomplete).
+static __device__ __noinline__ bool wait_bar(volatile int* abort_flag, char* ws, uint32_t bar, uint32_t parity) {
     if (*abort_flag) return false;
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const int limit = abort_flag[1];
     if (tc::mbar_wait(bar, parity, limit)) return true;
     report_timeout(ws, abort_flag);
     return false;
@@ -132,9 +136,8 @@ static __device__ __noinline__ bool wait_bar(volatile int* abort_flag, char* ws,
 struct Waiter {
     volatile int* abort_flag;
     char* ws;
-    int limit;  // polls per wait (the call's bound, from the workspace header)
     __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
-        return wait_bar(abort_flag, ws, bar, parity, limit);
+        return wait_bar(abort_flag, ws, bar, parity);
     }
 };
 
@@ -170,7 +173,9 @@ __device__ __forceinline__ void store_row64(uint32_t tile, uint32_t r, const flo
                          tc::pack_bf16(v[8 * j + 6], v[8 * j + 7]));
 }
 
-template <bool GDN>
+// MAXD: farthest 16-token block below the diagonal at which the inverse of
+// the delta system is formed (3: exact; 1: the block-adjacent solver).
+template <bool GDN, int MAXD>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
@@ -210,10 +215,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + kOffMisc);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + kOffMisc + 8);
-    const Waiter wait{abort_flag, ws, __shfl_sync(0xffffffffu, hdr->wait_limit, 0)};
+    const Waiter wait{abort_flag, ws};
 
     if (tid == 0) {
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        abort_flag[1] = hdr->wait_limit;
 #pragma unroll 1
         for (int b = 0; b < B_COUNT; ++b) tc::mbar_init(bar(b), b == B_FIN ? 4 : 1);
         tc::fence_mbar_init();
@@ -418,7 +424,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             tc::fence_proxy_async();
             tc::named_bar(1, 128);
-            if (GDN) tri_inverse_64(AF, scr, pw, lane, 1);
+            if (GDN) tri_inverse_64(AF, scr, pw, lane, 1, MAXD);
             // ---- TP[c & 1]: rows 0..63 T diag(beta e^g), rows 64..127 T diag(beta)
             if (c >= 2) wait(bar(B_TPF + (c & 1)), ((c >> 1) - 1) & 1);
             {
@@ -428,7 +434,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int jb = 0; jb < 4; ++jb) {
                     float v16[16];
-                    if (GDN && jb <= (t >> 4)) {
+                    if (GDN && jb <= (t >> 4) && (t >> 4) - jb <= MAXD) {
                         const float* Tr = tri_block_row(AF, t, jb);
 #pragma unroll
                         for (int e = 0; e < 16; e += 4) {
@@ -733,7 +739,8 @@ cudaError_t launch_fused(const PrefillArgs& a, cudaStream_t st) {
         mla = mq;
         mb = mq;
     }
-    auto kern = a.delta_rule ? prefill_kernel<true> : prefill_kernel<false>;
+    auto kern = !a.delta_rule ? prefill_kernel<false, 3>
+                              : a.max_block_dist == 1 ? prefill_kernel<true, 1> : prefill_kernel<true, 3>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)units, kThreads, kSmemAlloc, st>>>(mq, mk, mv, mla, mb, a.h0, (__nv_bfloat16*)a.o,

@@ -22,6 +22,10 @@ struct PrefillArgs {
     int H, dk, dv;
     gdn_dtype io;
     bool delta_rule;  // false: plain linear attention (no gates, no delta term)
+    // Farthest 16-token block below the diagonal at which the inverse of the
+    // delta system is kept: 3 = the exact solve (a 64-token chunk has four
+    // blocks), 1 = the block-adjacent solver.
+    int max_block_dist;
     void* o;
     float* h_T;
     char* ws;

@@ -122,7 +122,8 @@ template <typename IO, int DK, int DV>
 __global__ void __launch_bounds__(kStagedThreads)
 wy_kernel(const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ beta,
           int H, const char* __restrict__ ws, const float* __restrict__ g_in,
-          const float* __restrict__ A_in, float* __restrict__ w_out, float* __restrict__ u_out) {
+          const float* __restrict__ A_in, float* __restrict__ w_out, float* __restrict__ u_out,
+          int maxd) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     WySmem<IO, DK, DV>& s = *reinterpret_cast<WySmem<IO, DK, DV>*>(smem_raw);
     ChunkPos c;
@@ -165,18 +166,20 @@ wy_kernel(const IO* __restrict__ k, const IO* __restrict__ v, const float* __res
     }
     __syncthreads();
 
+    // T[i][j] for j at most maxd 16-token blocks before row i's block (all of
+    // them for the exact solve; the block-adjacent solver drops the rest)
     for (int e = tid; e < kChunk * DK; e += kStagedThreads) {
         int i = e / DK, x = e % DK;
         if (i >= c.n) continue;
         float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc = fmaf(s.T[i][j], s.kh[j][x], acc);
+        for (int j = max(0, (i >> 4) - maxd) << 4; j <= i; ++j) acc = fmaf(s.T[i][j], s.kh[j][x], acc);
         w_out[((size_t)(c.t0 + i) * H + h) * DK + x] = acc;
     }
     for (int e = tid; e < kChunk * DV; e += kStagedThreads) {
         int i = e / DV, y = e % DV;
         if (i >= c.n) continue;
         float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc = fmaf(s.T[i][j], s.vh[j][y], acc);
+        for (int j = max(0, (i >> 4) - maxd) << 4; j <= i; ++j) acc = fmaf(s.T[i][j], s.vh[j][y], acc);
         u_out[((size_t)(c.t0 + i) * H + h) * DV + y] = acc;
     }
 }
@@ -320,7 +323,8 @@ static cudaError_t wy_t(const PrefillArgs& a, const StagedBuffers& b, cudaStream
     cudaError_t e = set_smem(wy_kernel<IO, DK, DV>, sm);
     if (e != cudaSuccess) return e;
     wy_kernel<IO, DK, DV><<<grid, kStagedThreads, sm, st>>>((const IO*)a.k, (const IO*)a.v, a.beta,
-                                                            a.H, a.ws, b.g, b.A, b.w, b.u);
+                                                            a.H, a.ws, b.g, b.A, b.w, b.u,
+                                                            a.max_block_dist);
     return cudaGetLastError();
 }
 

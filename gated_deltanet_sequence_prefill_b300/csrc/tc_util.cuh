@@ -51,7 +51,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete: at most
 // `limit` polls (none when limit <= 0).  Returns false when the bound ran out
 // (the caller reports GDN_ERR_TIMEOUT).  kWaitLimit is the default bound; the
-// waits that drain copies already issued always use it.
+// waits that drain copies already issued always use it.  The fused kernels
+// poll once before they look up their bound (a phase already complete then
+// costs one poll), so their bound counts the polls after the first.
 constexpr int kWaitLimit = 1 << 22;
 // (the polling loops are kept rolled: unrolled, each copy cost kilobytes of
 // instruction footprint)

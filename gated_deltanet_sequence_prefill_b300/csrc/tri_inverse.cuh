@@ -35,9 +35,12 @@ __device__ __forceinline__ uint32_t tf32_bits(float x) { return __float_as_uint(
 
 // On entry M holds A below the diagonal (entries on and above it are never
 // read); on exit the layout above.  Called by the 128 threads of warps pw = 0..3 (warp index within the
-// group) with named barrier `bar_id`; `scratch` is 4 x 128 floats.
+// group) with named barrier `bar_id`; `scratch` is 4 x 128 floats.  Only the
+// blocks at most `maxd` blocks below the diagonal are formed (maxd = 3: the
+// whole inverse; maxd = 1: the block-adjacent solver, whose farther blocks
+// are taken as zero and never read).
 __device__ __forceinline__ void tri_inverse_64(float* M, float* scratch, int pw, int lane,
-                                               int bar_id) {
+                                               int bar_id, int maxd) {
     {
         float* B = M + (16 * pw) * kTriLd + 16 * pw;
         const int c = lane & 15;
@@ -68,7 +71,7 @@ __device__ __forceinline__ void tri_inverse_64(float* M, float* scratch, int pw,
     const int g = lane >> 2, t4 = lane & 3;
     float* scr = scratch + pw * 128;  // 16 x 8, row stride 8
 #pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
+    for (int d = 1; d <= maxd; ++d) {
 #pragma unroll 1
         for (int q = 0; q < 2; ++q) {
             const int tile = pw + 4 * q;

@@ -113,6 +113,26 @@ GDN_API gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
                          void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * GDN prefill with the block-adjacent solver of the SparseGDN article
+ * ("Двухуровневая разреженность SparseGDN…", first observation: the
+ * intra-chunk delta-system solve is restricted to links between
+ * neighbouring blocks, a fixed, input-independent approximation).  Each
+ * 64-token chunk is split into four blocks of 16 tokens; the inverse
+ * (I + A)^-1 of the delta system is formed exactly on the diagonal blocks
+ * and on the blocks right below them and taken as zero two or more blocks
+ * away (the rest of the computation is unchanged).  The result is an
+ * approximation of gdn_chunk_fwd's; its deviation depends on the input.
+ * Same arguments, layouts, workspace query (gdn_chunk_fwd_workspace_size)
+ * and error rules as gdn_chunk_fwd.
+ */
+GDN_API gdn_status gdn_chunk_fwd_block_adjacent(const void *q, const void *k, const void *v,
+                                        const float *log_alpha, const float *beta,
+                                        const float *h0, const int32_t *cu_seqlens, int n_seqs,
+                                        int64_t T_total, int H, int dk, int dv,
+                                        gdn_dtype io_dtype, void *o, float *h_T, void *workspace,
+                                        size_t ws_bytes, void *stream);
+
+/*
  * Plain causal linear attention S_t = S_{t-1} + v_t k_t^T, o_t = S_t q_t
  * ("Как ускорить LLM на длинном контексте", section "Linear attention"; the
  * reassociated evaluation order of "За пределами self-attention", section
@@ -219,8 +239,9 @@ GDN_API gdn_status gdn_workspace_status(const void *workspace, void *stream, int
  *  - gdn_set_wait_limit(polls) sets the bound for calls launched afterwards,
  *    process-wide, and returns the previous one.  The default is 4194304
  *    (1 << 22); polls < 0 restores it; polls = 0 makes every bounded wait
- *    give up at once (used by the tests to exercise the timeout path).  The
- *    outputs of a call that timed out are unspecified.
+ *    that finds its barrier incomplete at its first poll give up at once
+ *    (used by the tests to exercise the timeout path).  The outputs of a
+ *    call that timed out are unspecified.
  *  - gdn_workspace_timeout_site() waits for `stream`, then reads which
  *    barrier the first timed-out wait of the call gave up on (0: none;
  *    1000 + index on a solve CTA, 2000 + index on a state CTA of the cluster

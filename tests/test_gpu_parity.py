@@ -259,6 +259,60 @@ def test_gdn_single_sequence_t131072_h32(g):
     check_chains(inp, o, hT, [(0, 0), (0, 13), (0, 22), (0, 31)], TOL["bf16"])
 
 
+# ------------------------------------------------------------------ block-adjacent solver
+
+def ref_band(inp, **kw):
+    return oracle.chunked(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"], inp["h0"],
+                          inp["cu_seqlens"], band=16, **kw)
+
+
+@pytest.mark.parametrize("dk,dv,dtype", [(64, 64, "fp32"), (128, 128, "fp32"), (64, 128, "fp32"),
+                                         (128, 64, "bf16"), (128, 128, "bf16")])
+def test_block_adjacent_against_oracle(g, dk, dv, dtype):
+    """gdn_chunk_fwd_block_adjacent against the oracle's block-adjacent solve
+    (16-token blocks), at the dtype's tolerance; the approximation itself is
+    far outside that tolerance from the exact solve on these inputs, so the
+    comparison tells the two apart."""
+    inp = gi.gdn_inputs([300, 77, 0, 129, 1], 4, dk, dv, dtype, h0_std=0.01, seed=31)
+    o, hT = run_gdn(g, inp, block_adjacent=True)
+    ob, hb = ref_band(inp)
+    assert rel(o, ob) <= TOL[dtype], rel(o, ob)
+    assert rel(hT, hb) <= TOL[dtype], rel(hT, hb)
+    oe, _ = ref_gdn(inp)
+    assert rel(ob, oe) > 2 * TOL[dtype]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("scale", [1.0, 40.0])
+def test_block_adjacent_fused_kernels(g, monkeypatch, kernel, scale):
+    """The block-adjacent solve in each fused kernel (ordinary gates, and
+    strong ones that take the kernels' large-decay path)."""
+    use_kernel(monkeypatch, kernel)
+    inp = gi.gdn_inputs([700, 63, 200], 4, 128, 128, "bf16", h0_std=0.01, seed=32)
+    inp["log_alpha"] = inp["log_alpha"] * scale
+    o, hT = run_gdn(g, inp, block_adjacent=True)
+    ob, hb = ref_band(inp)
+    assert rel(o, ob) <= TOL["bf16"] and rel(hT, hb) <= TOL["bf16"], (rel(o, ob), rel(hT, hb))
+
+
+def test_block_adjacent_varlen_t131072_h32(g):
+    """The benchmarked packed call (4 sequences, 131072 tokens, H = 32) with
+    the block-adjacent solve; every token of sampled heads of the shortest
+    sequence against the oracle's banded solve, and their final states."""
+    lengths = gi.varlen_lengths(131072, 4, 0)
+    inp = gi.gdn_inputs(lengths, 32, 128, 128, "bf16", h0_std=0.01, seed=0)
+    o, hT = run_gdn(g, inp, block_adjacent=True)
+    s = int(np.argmin(lengths))
+    cu = inp["cu_seqlens"].tolist()
+    a, e = cu[s], cu[s + 1]
+    hs = [0, 11, 31]
+    sub = {k: inp[k][a:e, hs] for k in ("q", "k", "v", "log_alpha", "beta")}
+    sub["h0"] = inp["h0"][s:s + 1, hs]
+    sub["cu_seqlens"] = None
+    ob, hb = ref_band(sub)
+    assert rel(o[a:e, hs], ob) <= TOL["bf16"] and rel(hT[s, hs], hb[0]) <= TOL["bf16"]
+
+
 # ------------------------------------------------------------------ failure detection
 
 @pytest.mark.parametrize("kernel", KERNELS)
