@@ -7,7 +7,7 @@ larger than L2 (4.35 GB), so no L2 flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --workload {gdn_t32768_h16, gdn_t131072_h32_single, gdn_t65536_h8, linear_b2_t4096_h8,
-                              decode_b128_h32, gdn_varlen_t131072_h32_block_adjacent}
+                              decode_b128_h32, gdn_varlen_t131072_h32_block_adjacent, gdn_t131072_h4}
                                                    (the other workloads, one GPU)
 
 One JSON line is printed by rank 0.  Under torchrun each rank runs the same
@@ -415,6 +415,9 @@ def run_workload(args):
         elif name == "gdn_t16384_h4":  # the same length with few units
             lengths, Hh, kind = [16384], 4, "gdn"
             inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
+        elif name == "gdn_t131072_h4":  # one long sequence, few heads: the two-level state scan
+            lengths, Hh, kind = [131072], 4, "gdn"
+            inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
         elif name == "gdn_varlen_t131072_h32_block_adjacent":  # the headline with the approximate solver
             lengths, Hh, kind = LENGTHS, H, "gdn_block_adjacent"
             inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
@@ -440,8 +443,10 @@ def run_workload(args):
         units, unit = Tt, "tokens/s"
         bytes_per_call = 4 * Tt * Hh * D * 2 + (2 * Tt * Hh * 4 if gdn_kind else 0) + \
             (2 if gdn_kind else 1) * nn * Hh * D * D * 4
-        launches = 2
+        segs = g.two_level_segments(Tt, Hh, nn, delta_rule=gdn_kind)
+        launches = 2 if segs < 2 else (7 if gdn_kind else 6)
         cfg = {"workload": name, "T": Tt, "H": Hh, "dk": D, "dv": D, "seq_lens": lengths,
+               "two_level_segments": segs,
                "chunk": 64, "path": kernel_name(True, nn * Hh), "l2": ("L2 flushed (256 MB write) between timed calls"
                                    if flush is not None else "inputs larger than L2, no flush")}
     for _ in range(args.warmup):

@@ -55,6 +55,8 @@ lib.gdn_workspace_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
 lib.gdn_workspace_status.restype = _i
 lib.gdn_workspace_timeout_site.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
 lib.gdn_workspace_timeout_site.restype = _i
+lib.gdn_prefill_segments.argtypes = [_i64, _i, _i, _i, _i, _i, _i]
+lib.gdn_prefill_segments.restype = _i
 lib.gdn_set_wait_limit.argtypes = [_i]
 lib.gdn_set_wait_limit.restype = _i
 
@@ -264,3 +266,9 @@ def set_wait_limit(polls):
     calls launched from now on (process-wide); negative restores the default.
     Returns the previous bound."""
     return int(lib.gdn_set_wait_limit(int(polls)))
+
+
+def two_level_segments(T, H, n_seqs, dk=128, dv=128, dtype=torch.bfloat16, delta_rule=True):
+    """Segments per sequence a prefill call of these sizes takes (1: one pass)."""
+    io = GDN_BF16 if dtype == torch.bfloat16 else GDN_FP32
+    return int(lib.gdn_prefill_segments(T, H, dk, dv, n_seqs, io, int(bool(delta_rule))))

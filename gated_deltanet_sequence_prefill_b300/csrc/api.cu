@@ -12,6 +12,28 @@
 
 using namespace gdn;
 
+namespace gdn {
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// Solve CTAs per cluster for the cluster kernel: two (a 3-SM cluster) when
+// every (sequence, head) then still has its cluster at once, else one (more
+// clusters side by side pay off more than a faster solve).
+// GDN_PREFILL_FRONTS=1 or 2 in the environment forces the choice.
+int pair_fronts(const PrefillArgs& a) {
+    const char* e = getenv("GDN_PREFILL_FRONTS");
+    if (e != nullptr && (e[0] == '1' || e[0] == '2')) return e[0] - '0';
+    return 3LL * a.n_seqs * a.H <= (long long)sm_count() ? 2 : 1;
+}
+
+}  // namespace gdn
+
 namespace {
 
 // Polls per bounded device wait, for the calls launched from now on.
@@ -80,6 +102,7 @@ PrefillArgs make_args(const void* q, const void* k, const void* v, const float* 
     a.cu_seqlens = cu; a.n_seqs = n_seqs; a.T_total = T; a.H = H; a.dk = dk; a.dv = dv;
     a.io = io; a.delta_rule = delta; a.o = o; a.h_T = h_T; a.ws = (char*)ws;
     a.max_block_dist = 3;
+    a.mode = 0;
     return a;
 }
 
@@ -93,26 +116,16 @@ bool use_pair(const PrefillArgs& a) {
     return !(e != nullptr && e[0] == '0');
 }
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return 0;
-    return n;
-}
-
-// Solve CTAs per cluster for the cluster kernel: two (a 3-SM cluster) when
-// every (sequence, head) then still has its cluster at once, else one (more
-// clusters side by side pay off more than a faster solve).
-// GDN_PREFILL_FRONTS=1 or 2 in the environment forces the choice.
-int pair_fronts(const PrefillArgs& a) {
-    const char* e = getenv("GDN_PREFILL_FRONTS");
-    if (e != nullptr && (e[0] == '1' || e[0] == '2')) return e[0] - '0';
-    return 3LL * a.n_seqs * a.H <= (long long)sm_count() ? 2 : 1;
-}
-
 gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
     const bool pair = use_pair(a);
+    if (pair) {
+        const int G = two_level_segments(a);
+        if (G >= 2) {
+            gdn_status s = check_prefill(a, ws_bytes, two_level_workspace_bytes(a.n_seqs, a.H, G), true);
+            if (s != GDN_OK) return s;
+            return cuda_status(launch_two_level(a, G, g_wait_limit.load(), st));
+        }
+    }
     const bool fused = pair || fused_supported(a);
     size_t need = pair ? pair_workspace_bytes(a.n_seqs, a.H) : plan_bytes(a.n_seqs);
     if (!fused) need += staged_intermediate_bytes(a.T_total, a.H, a.dk, a.dv, a.n_seqs);
@@ -168,7 +181,10 @@ size_t gdn_chunk_fwd_workspace_size(int64_t T, int H, int dk, int dv, int n_seqs
     if (!sizes_ok(T, H, dk, dv, n_seqs) || (io != GDN_BF16 && io != GDN_FP32)) return 0;
     PrefillArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, n_seqs,
                               T, H, dk, dv, io, true, nullptr, nullptr, nullptr);
-    if (pair_shape_ok(a)) return pair_workspace_bytes(n_seqs, H);
+    if (pair_shape_ok(a)) {
+        const int G = two_level_segments(a);
+        return G >= 2 ? two_level_workspace_bytes(n_seqs, H, G) : pair_workspace_bytes(n_seqs, H);
+    }
     if (fused_supported(a)) return plan_bytes(n_seqs);
     return gdn_staged_workspace_size(T, H, dk, dv, n_seqs, io);
 }
@@ -177,9 +193,19 @@ size_t linear_attn_fwd_workspace_size(int64_t T, int H, int dk, int dv, int n_se
     if (!sizes_ok(T, H, dk, dv, n_seqs) || (io != GDN_BF16 && io != GDN_FP32)) return 0;
     PrefillArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, n_seqs,
                               T, H, dk, dv, io, false, nullptr, nullptr, nullptr);
-    if (pair_shape_ok(a)) return pair_workspace_bytes(n_seqs, H);
+    if (pair_shape_ok(a)) {
+        const int G = two_level_segments(a);
+        return G >= 2 ? two_level_workspace_bytes(n_seqs, H, G) : pair_workspace_bytes(n_seqs, H);
+    }
     if (fused_supported(a)) return plan_bytes(n_seqs);
     return gdn_staged_workspace_size(T, H, dk, dv, n_seqs, io);
+}
+
+int gdn_prefill_segments(int64_t T, int H, int dk, int dv, int n_seqs, gdn_dtype io, int delta_rule) {
+    if (!sizes_ok(T, H, dk, dv, n_seqs) || (io != GDN_BF16 && io != GDN_FP32)) return 0;
+    PrefillArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, n_seqs,
+                              T, H, dk, dv, io, delta_rule != 0, nullptr, nullptr, nullptr);
+    return two_level_segments(a);
 }
 
 gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha,

@@ -64,6 +64,8 @@ bool encode_gate_map(CUtensorMap* m, const float* ptr, int64_t T, int H);
 namespace pair {
 
 constexpr int kThreads = 512;  // 16 warps in both CTAs
+// run-mode bits (PrefillArgs::mode)
+constexpr int kModeNoOutput = 1, kModeZeroV = 2, kModeIdentityH0 = 4;
 constexpr int kD = 128;
 
 // ---------------------------------------------------------------- front layout
@@ -281,7 +283,8 @@ __device__ __noinline__ void derive_gates(const float* la_raw, const float* b_ra
 
 // MAXD: farthest 16-token block below the diagonal at which the inverse of
 // the delta system is formed (3: exact; 1: the block-adjacent solver).
-template <bool GDN, int FR, int MAXD>
+// MODE: run-mode bits of the two-level state scan (0 for an ordinary call).
+template <bool GDN, int FR, int MAXD, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_la,
@@ -326,7 +329,19 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + (front ? kFBar : kBBar) + kBarSlots * 8);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sptr + (front ? kFBar : kBBar) + kBarSlots * 8 + 8);
     const Waiter wait{abort_flag, ws, bar_base, front ? 1000 : 2000};
+    // run modes of the two-level state scan (0 for an ordinary call): no o
+    // stores; v taken as zero; h0 taken as the identity
+    constexpr bool no_o = (MODE & kModeNoOutput) != 0;
+    constexpr bool vzero = (MODE & kModeZeroV) != 0;
+    constexpr bool h0eye = (MODE & kModeIdentityH0) != 0;
 
+    if (!front && vzero) {  // the v tiles of both apply entries hold zeros for the whole run
+        for (uint32_t x = tid; x < 2 * 2 * kBBox / 16; x += kThreads) {
+            const uint32_t ent = x / (2 * kBBox / 16), off = (x % (2 * kBBox / 16)) * 16;
+            tc::st_shared_v4(sbase + kARing + ent * kAEntry + kAV + off, 0u, 0u, 0u, 0u);
+        }
+        tc::fence_proxy_async();
+    }
     if (tid == 0) {
         abort_flag[0] = 0;
         abort_flag[1] = hdr->wait_limit;
@@ -645,12 +660,14 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     tc::tma_load_3d(ce + kCQ + kBBox, &tm_q, 64, head, t0, bar(B_FULLC + e));
                     tc::tma_load_3d(ce + kCK, &tm_k, 0, head, t0, bar(B_FULLC + e));
                     tc::tma_load_3d(ce + kCK + kBBox, &tm_k, 64, head, t0, bar(B_FULLC + e));
-                    tc::mbar_arrive_expect_tx(bar(B_FULLA + a), 2 * 8192 + (GDN ? 1024 : 0));
-                    tc::tma_load_3d(ae + kAV, &tm_v, 0, head, t0, bar(B_FULLA + a));
-                    tc::tma_load_3d(ae + kAV + kBBox, &tm_v, 64, head, t0, bar(B_FULLA + a));
+                    tc::mbar_arrive_expect_tx(bar(B_FULLA + a), (vzero ? 0 : 2 * 8192) + (GDN ? 1024 : 0));
+                    if (!vzero) {
+                        tc::tma_load_3d(ae + kAV, &tm_v, 0, head, t0, bar(B_FULLA + a));
+                        tc::tma_load_3d(ae + kAV + kBBox, &tm_v, 64, head, t0, bar(B_FULLA + a));
+                    }
                     if (GDN) tc::tma_load_2d(ae + kALa, &tm_la, head & ~3, t0, bar(B_FULLA + a));
                     issued = c + 1;
-                    if (c + 2 < nch) {
+                    if (c + 2 < nch && !vzero) {
                         const int tp = t0 + 2 * kChunk;
                         tc::tma_prefetch_3d(&tm_v, 0, head, tp);
                         tc::tma_prefetch_3d(&tm_v, 64, head, tp);
@@ -724,7 +741,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 if (ostore) {
                     tc::mbar_arrive(bar(B_D1OF + b));
                     if (full) {
-                        if (!*abort_flag) {
+                        if (!*abort_flag && !no_o) {
                             tc::tma_store_3d(&tm_o, ce + kCK, 0, head, t0);
                             tc::tma_store_3d(&tm_o, ce + kCK + kBBox, 64, head, t0);
                             tc::bulk_commit();
@@ -735,7 +752,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
                 __syncwarp();
                 if (!full) {
-                    if (!*abort_flag) {
+                    if (!*abort_flag && !no_o) {
 #pragma unroll 1
                         for (int t = 0; t < n; ++t)
                             o[((size_t)(t0 + t) * H + head) * kD + j] = __float2bfloat16_rn(xs[t]);
@@ -823,7 +840,8 @@ pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     uint32_t r[16];
 #pragma unroll
                     for (int x = 0; x < 16; ++x)
-                        r[x] = __float_as_uint((h0 && !dead) ? h0[hbase + (size_t)(64 * hh + 16 * part + x) * kD + j] : 0.f);
+                        r[x] = __float_as_uint(h0eye ? (64 * hh + 16 * part + x == j ? 1.f : 0.f)
+                                               : (h0 && !dead) ? h0[hbase + (size_t)(64 * hh + 16 * part + x) * kD + j] : 0.f);
                     tc::tmem_st16(d2 + 16 * part, r);
                 }
                 tc::tmem_wait_st();
@@ -1006,6 +1024,30 @@ bool pair_supported(const PrefillArgs& a) {
     return al(a.q, 16) && al(a.k, 16) && al(a.v, 16) && tensor_map_encoder() != nullptr;
 }
 
+// The instantiation for a call: the ordinary prefill (exact or block-adjacent
+// solve, GDN or linear attention), or one of the runs of the two-level state
+// scan (transition maps: no o, v = 0, h0 = I; offsets: no o).
+using PairKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                            const float*, __nv_bfloat16*, float*, char*, char*, int);
+template <int FR>
+static PairKernel pick_fr(const PrefillArgs& a) {
+    using namespace pair;
+    constexpr int kMaps = kModeNoOutput | kModeZeroV | kModeIdentityH0;
+    if (!a.delta_rule) {
+        if (a.mode == 0) return pair_kernel<false, FR, 3, 0>;
+        if (a.mode == kModeNoOutput) return pair_kernel<false, FR, 3, kModeNoOutput>;
+        return nullptr;
+    }
+    if (a.mode == 0) return a.max_block_dist == 1 ? pair_kernel<true, FR, 1, 0> : pair_kernel<true, FR, 3, 0>;
+    if (a.max_block_dist != 3) return nullptr;
+    if (a.mode == kModeNoOutput) return pair_kernel<true, FR, 3, kModeNoOutput>;
+    if (a.mode == kMaps) return pair_kernel<true, FR, 3, kMaps>;
+    return nullptr;
+}
+static PairKernel pick_kernel(const PrefillArgs& a, int fronts) {
+    return fronts == 2 ? pick_fr<2>(a) : pick_fr<1>(a);
+}
+
 cudaError_t launch_pair(const PrefillArgs& a, int fronts, cudaStream_t st) {
     using namespace pair;
     const long long units = (long long)a.n_seqs * a.H;
@@ -1026,11 +1068,8 @@ cudaError_t launch_pair(const PrefillArgs& a, int fronts, cudaStream_t st) {
         mla = mq;
         mb = mq;
     }
-    const bool band = a.delta_rule && a.max_block_dist == 1;
-    auto kern = fronts == 2 ? (band ? pair_kernel<true, 2, 1>
-                                    : a.delta_rule ? pair_kernel<true, 2, 3> : pair_kernel<false, 2, 3>)
-                            : (band ? pair_kernel<true, 1, 1>
-                                    : a.delta_rule ? pair_kernel<true, 1, 3> : pair_kernel<false, 1, 3>);
+    auto kern = pick_kernel(a, fronts);
+    if (kern == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

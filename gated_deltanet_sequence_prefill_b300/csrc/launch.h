@@ -26,6 +26,10 @@ struct PrefillArgs {
     // delta system is kept: 3 = the exact solve (a 64-token chunk has four
     // blocks), 1 = the block-adjacent solver.
     int max_block_dist;
+    // Runs of the two-level state scan use the cluster kernel with these bits
+    // (0 for an ordinary call): 1 = o is not stored; 2 = v is taken as zero;
+    // 4 = h0 is taken as the identity (dk = dv).
+    int mode;
     void* o;
     float* h_T;
     char* ws;
@@ -44,9 +48,12 @@ size_t staged_intermediate_bytes(int64_t T, int H, int dk, int dv, int n_seqs);
 StagedBuffers staged_buffers(char* ws, int64_t T, int H, int dk, int dv, int n_seqs);
 
 // wait_limit: polls a bounded device wait of the call's kernels makes before
-// it reports GDN_ERR_TIMEOUT (recorded in the workspace header).
+// it reports GDN_ERR_TIMEOUT (recorded in the workspace header).  upstream
+// (device, may be NULL): a status word found earlier in the same call; if it
+// is not GDN_OK the plan carries it, and the kernels reading the plan skip
+// their work.
 cudaError_t launch_plan(const int32_t* cu, int n_seqs, int64_t T_total, int wait_limit, void* ws,
-                        cudaStream_t st);
+                        cudaStream_t st, const int* upstream = nullptr);
 cudaError_t launch_kkt(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
 cudaError_t launch_wy(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
 cudaError_t launch_state_ffma(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
@@ -66,5 +73,13 @@ bool pair_supported(const PrefillArgs& a);
 size_t pair_workspace_bytes(int n_seqs, int H);  // plan + global scratch
 // fronts: solve CTAs per cluster (1 or 2), next to the one state CTA.
 cudaError_t launch_pair(const PrefillArgs& a, int fronts, cudaStream_t st);
+// Solve CTAs per cluster the cluster kernel takes for these arguments.
+int pair_fronts(const PrefillArgs& a);
+
+// Two-level state scan (long sequences with few (sequence, head) chains):
+// segments per sequence the call takes (1: none), its workspace, its launch.
+int two_level_segments(const PrefillArgs& a);
+size_t two_level_workspace_bytes(int n_seqs, int H, int G);
+cudaError_t launch_two_level(const PrefillArgs& a, int G, int wait_limit, cudaStream_t st);
 
 }  // namespace gdn

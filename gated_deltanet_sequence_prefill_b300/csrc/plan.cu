@@ -11,7 +11,8 @@ constexpr int kPlanThreads = 1024;
 constexpr int kOrderQuadraticMax = 4096;  // above this, keep the natural order
 
 __global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs, long long T_total, int wait_limit, char* ws) {
+plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs, long long T_total, int wait_limit, char* ws,
+            const int* __restrict__ upstream) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
     PlanLayout L(n_seqs);
     int* cu = reinterpret_cast<int*>(ws + L.cu);
@@ -81,7 +82,8 @@ plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs, long long T_total, in
         order[rank] = i;
     }
     if (tid == 0) {
-        hdr->status = GDN_OK;
+        // a call whose own inputs were already found bad upstream does nothing
+        hdr->status = (upstream != nullptr && *upstream != GDN_OK) ? *upstream : GDN_OK;
         hdr->counter = 0;
         hdr->timeout_site = 0;
         hdr->wait_limit = wait_limit;
@@ -92,8 +94,8 @@ plan_kernel(const int32_t* __restrict__ cu_in, int n_seqs, long long T_total, in
 }
 
 cudaError_t launch_plan(const int32_t* cu, int n_seqs, int64_t T_total, int wait_limit, void* ws,
-                        cudaStream_t st) {
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(cu, n_seqs, (long long)T_total, wait_limit, (char*)ws);
+                        cudaStream_t st, const int* upstream) {
+    plan_kernel<<<1, kPlanThreads, 0, st>>>(cu, n_seqs, (long long)T_total, wait_limit, (char*)ws, upstream);
     return cudaGetLastError();
 }
 

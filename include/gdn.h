@@ -113,6 +113,27 @@ GDN_API gdn_status gdn_chunk_fwd(const void *q, const void *k, const void *v,
                          void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Long sequences with few (sequence, head) chains: the two-level state scan.
+ * A chunk acts on the state as an affine map h -> M h + B (SparseGDN
+ * article, "Схема встраивания селектора…"), and so does a run of chunks.
+ * When a gdn_chunk_fwd / linear_attn_fwd call of the cluster kernel's shapes
+ * (bf16, dk = dv = 128) has few chains (at most 9) and sequences long
+ * enough for at least 5 segments of 32 chunks, it
+ * cuts every sequence into G segments of whole chunks, forms every segment's
+ * map in parallel (two extra passes over the segments, without outputs; one
+ * for linear attention, whose M is the identity), composes the maps in
+ * segment order into each segment's starting state and the final state, and
+ * then computes the outputs of all segments in parallel.  The result is the
+ * same as the one-pass evaluation up to rounding; the workspace query
+ * includes the extra space.  gdn_prefill_segments() returns the G a call of
+ * these sizes takes (1: the one-pass evaluation; 0: bad sizes).  In the
+ * environment, GDN_TWO_LEVEL=0 turns the scan off and GDN_TWO_LEVEL=G
+ * (2..64) forces G segments for the shapes that support it.
+ */
+GDN_API int gdn_prefill_segments(int64_t T_total, int H, int dk, int dv, int n_seqs,
+                                 gdn_dtype io_dtype, int delta_rule);
+
+/*
  * GDN prefill with the block-adjacent solver of the SparseGDN article
  * ("Двухуровневая разреженность SparseGDN…", first observation: the
  * intra-chunk delta-system solve is restricted to links between

@@ -122,3 +122,21 @@ def test_wait_limit_setter(g):
     assert g.set_wait_limit(12345) == 0
     assert g.set_wait_limit(-1) == 12345
     assert g.set_wait_limit(-1) == default
+
+
+def test_workspace_query_covers_the_two_level_scan(g, monkeypatch):
+    # few long chains: the query includes the scan's runs and maps
+    T, H, N = 131072, 4, 1
+    monkeypatch.setenv("GDN_TWO_LEVEL", "0")
+    plain = g.chunk_fwd_workspace_size(T, H, 128, 128, N)
+    monkeypatch.delenv("GDN_TWO_LEVEL")
+    scan = g.chunk_fwd_workspace_size(T, H, 128, 128, N)
+    assert plain < N * H * 192 * 1024 + (1 << 20)
+    # G segments per sequence: cluster scratch plus M, B and h_start (64 KB each) per segment and head
+    G = min(16, 37 // (N * H) + 1)
+    assert scan >= N * G * H * (192 + 3 * 64) * 1024
+    monkeypatch.setenv("GDN_TWO_LEVEL", "5")
+    assert g.chunk_fwd_workspace_size(T, H, 128, 128, N) >= N * 5 * H * (192 + 3 * 64) * 1024
+    # many chains: no scan
+    monkeypatch.delenv("GDN_TWO_LEVEL")
+    assert g.chunk_fwd_workspace_size(T, 32, 128, 128, 4) < 4 * 32 * 192 * 1024 + (1 << 20)

@@ -313,6 +313,83 @@ def test_block_adjacent_varlen_t131072_h32(g):
     assert rel(o[a:e, hs], ob) <= TOL["bf16"] and rel(hT[s, hs], hb[0]) <= TOL["bf16"]
 
 
+# ------------------------------------------------------------------ two-level state scan
+
+@pytest.mark.parametrize("G", ["2", "5"])
+@pytest.mark.parametrize("delta", [True, False])
+def test_two_level_scan_against_oracle(g, monkeypatch, G, delta):
+    """The two-level state scan forced to G segments per sequence (transition
+    maps and offsets of all segments side by side, a scan of the maps, then
+    the outputs from the segment starts) on ragged packed sequences: every
+    token and every final state against the oracle."""
+    monkeypatch.setenv("GDN_TWO_LEVEL", G)
+    lengths = [700, 1, 0, 333, 2000]
+    if delta:
+        inp = gi.gdn_inputs(lengths, 4, 128, 128, "bf16", h0_std=0.01, seed=41)
+        o, hT = run_gdn(g, inp)
+        ro, rh = ref_gdn(inp)
+    else:
+        inp = gi.linear_inputs(lengths, 4, 128, 128, "bf16", h0_std=0.5, seed=42)
+        d = dev(inp)
+        o, hT, ws = g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"])
+        assert g.workspace_status(ws) == 0
+        ro, rh = oracle.linear(inp["q"], inp["k"], inp["v"], inp["h0"], inp["cu_seqlens"])
+    assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
+    assert rel(hT, rh) <= TOL["bf16"], rel(hT, rh)
+
+
+def test_two_level_scan_without_h0_or_final_state(g, monkeypatch):
+    monkeypatch.setenv("GDN_TWO_LEVEL", "3")
+    inp = gi.gdn_inputs([900, 130], 4, 128, 128, "bf16", h0_std=0.0, seed=43)
+    d = dev(inp)
+    o, hT, ws = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], None,
+                                d["cu_seqlens"], output_final_state=False)
+    assert hT is None and g.workspace_status(ws) == 0
+    ro, _ = oracle.gdn(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"], None,
+                       inp["cu_seqlens"])
+    assert rel(o, ro) <= TOL["bf16"]
+
+
+def test_two_level_scan_reports_malformed_seqlens(g, monkeypatch):
+    monkeypatch.setenv("GDN_TWO_LEVEL", "4")
+    inp = gi.gdn_inputs([64, 64], 4, 128, 128, "bf16", h0_std=0.0, seed=44)
+    d = dev(inp)
+    cu = torch.tensor([0, 100, 64], dtype=torch.int32, device="cuda")
+    _, _, ws = g.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], None, cu)
+    assert g.workspace_status(ws) == -4
+
+
+def test_two_level_scan_forced_timeout_then_recovery(g, monkeypatch):
+    """Every bounded wait gives up at once in the scan's runs: the call ends
+    with GDN_ERR_TIMEOUT and a barrier site in the caller's workspace, and a
+    normal call on the same workspace then matches the oracle."""
+    monkeypatch.setenv("GDN_TWO_LEVEL", "3")
+    inp = gi.gdn_inputs([500, 257], 4, 128, 128, "bf16", h0_std=0.01, seed=45)
+    d = dev(inp)
+    args = [d[k] for k in ("q", "k", "v", "log_alpha", "beta", "h0", "cu_seqlens")]
+    old = g.set_wait_limit(0)
+    try:
+        _, _, ws = g.gdn_chunk_fwd(*args)
+        assert g.workspace_status(ws) == -9
+        assert g.workspace_timeout_site(ws) != 0
+    finally:
+        g.set_wait_limit(old)
+    o, hT, _ = g.gdn_chunk_fwd(*args, workspace=ws)
+    assert g.workspace_status(ws) == 0
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
+
+
+def test_two_level_scan_default_t131072_h4(g, monkeypatch):
+    """A 131072-token sequence with 4 heads: the automatic choice cuts it into
+    segments (4 chains alone would keep 12 of the SMs busy).  Two heads,
+    every token, and all final states against the oracle."""
+    monkeypatch.delenv("GDN_TWO_LEVEL", raising=False)
+    inp = gi.gdn_inputs([131072], 4, 128, 128, "bf16", h0_std=0.01, seed=0)
+    o, hT = run_gdn(g, inp)
+    check_chains(inp, o, hT, [(0, 1), (0, 3)], TOL["bf16"])
+
+
 # ------------------------------------------------------------------ failure detection
 
 @pytest.mark.parametrize("kernel", KERNELS)
