@@ -13,6 +13,13 @@ What it computes (the readings are listed with the C source, gdn_oracle.c):
   chunked(...)    the chunk-wise evaluation (intra-chunk delta-system solve,
                   sequential pass over chunks, outputs from chunk-start states:
                   SparseGDN article, "Чем дорог префилл в Gated Delta Networks…")
+  linear_variant(...)  linear attention with the causal mask optional and the
+                  normaliser optional: o_t = sum_s w_ts v_s with w_ts = q_t . k_s
+                  over s <= t (causal) or all s of the sequence (bidirectional),
+                  divided by sum_s w_ts when normalised (datadaily.news
+                  "За пределами self-attention", section "Линейное внимание…",
+                  the normalised listing; ai-vestnik.ru item on linear attention:
+                  the bidirectional mode and the causal restriction).
   linear_quadratic(...)  the quadratic masked form (Q K^T ⊙ M) V + Q h0 of
                   causal linear attention (datadaily.news "За пределами
                   self-attention", section "Линейное внимание…": the two
@@ -220,3 +227,35 @@ def linear_quadratic(q, k, v, h0=None, cu_seqlens=None):
             o[a:e, h] = out
             hT[s, h] = st
     return o, hT
+
+
+def linear_variant(q, k, v, cu_seqlens=None, causal=True, normalize=False):
+    """Linear attention in its quadratic form, per sequence and head, fp64:
+        W = Q K^T, masked to s <= t when causal (diagonal included);
+        o = W V, divided row by row by W 1 when normalised.
+    Also returns, per sequence and head, kv = K^T V (dk x dv, the summed
+    state) and z = K^T 1 (the summed keys).  The feature map (elu + 1 on the
+    page) is applied by the caller to q and k beforehand; no epsilon is added
+    to the normaliser (the page adds none)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    N = len(cu) - 1
+    o = np.zeros((T, H, dv))
+    kv = np.zeros((N, H, dk, dv))
+    z = np.zeros((N, H, dk))
+    for s in range(N):
+        a, e = int(cu[s]), int(cu[s + 1])
+        for h in range(H):
+            Q, K, V = q[a:e, h], k[a:e, h], v[a:e, h]
+            W = Q @ K.T
+            if causal:
+                W = W * np.tril(np.ones((e - a, e - a)))
+            out = W @ V
+            if normalize:
+                out = out / W.sum(axis=1, keepdims=True)
+            o[a:e, h] = out
+            kv[s, h] = K.T @ V
+            z[s, h] = K.sum(axis=0)
+    return o, kv, z

@@ -303,6 +303,89 @@ def test_block_adjacent_keeps_exactly_the_two_diagonals_of_blocks():
         np.testing.assert_allclose(bd["u"][a:e, 0], Tb @ (b[a:e, 0, None] * v[a:e, 0]), rtol=0, atol=1e-12)
 
 
+# --- linear-attention variants: causal or bidirectional, normalised or not ---
+
+def _positive_case(rng, lengths, H, dk, dv):
+    T = sum(lengths)
+    elu1 = lambda x: np.where(x > 0, x + 1.0, np.exp(x))  # elu(x) + 1 > 0
+    q = elu1(rng.standard_normal((T, H, dk)))
+    k = elu1(rng.standard_normal((T, H, dk)))
+    v = rng.standard_normal((T, H, dv))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    return q, k, v, cu
+
+
+def test_linear_variants_brute_force():
+    """Element by element: o_t[j] = sum_s (q_t . k_s) v_s[j] / sum_s (q_t . k_s)
+    over the causal or the whole range, with explicit loops."""
+    rng = np.random.default_rng(31)
+    q, k, v, cu = _positive_case(rng, [5, 0, 3], 2, 3, 2)
+    for causal in (True, False):
+        for norm in (True, False):
+            o, kv, z = oracle.linear_variant(q, k, v, cu, causal=causal, normalize=norm)
+            for sq in range(2):
+                a, e = int(cu[sq]), int(cu[sq + 1])
+                for h in range(2):
+                    for t in range(a, e):
+                        top = np.zeros(2)
+                        bot = 0.0
+                        for u in range(a, (t + 1) if causal else e):
+                            w = sum(q[t, h, x] * k[u, h, x] for x in range(3))
+                            top += w * v[u, h]
+                            bot += w
+                        ref = top / bot if norm else top
+                        np.testing.assert_allclose(o[t, h], ref, rtol=1e-13, atol=1e-13)
+                    np.testing.assert_allclose(z[sq, h], k[a:e, h].sum(axis=0), rtol=1e-13)
+                    ref_kv = sum(np.outer(k[u, h], v[u, h]) for u in range(a, e)) if e > a else 0.0
+                    np.testing.assert_allclose(kv[sq, h], ref_kv, rtol=1e-13, atol=1e-13)
+
+
+def test_normalised_weights_sum_to_one():
+    """With positive features the normalised weights of a token sum to one, so
+    a value that is the same vector c for every token comes out as c."""
+    rng = np.random.default_rng(32)
+    q, k, v, cu = _positive_case(rng, [40, 7], 3, 8, 5)
+    c = rng.standard_normal(5)
+    v[:] = c
+    for causal in (True, False):
+        o, _, _ = oracle.linear_variant(q, k, v, cu, causal=causal, normalize=True)
+        np.testing.assert_allclose(o, np.broadcast_to(c, o.shape), rtol=1e-12, atol=1e-12)
+
+
+def test_causal_variants_first_token_and_recurrence():
+    """The causal normalised output of a sequence's first token is its own
+    value; the causal unnormalised output is the plain recurrence."""
+    rng = np.random.default_rng(33)
+    q, k, v, cu = _positive_case(rng, [12, 1, 9], 2, 4, 3)
+    o, _, _ = oracle.linear_variant(q, k, v, cu, causal=True, normalize=True)
+    for sq in range(3):
+        a = int(cu[sq])
+        np.testing.assert_allclose(o[a], v[a], rtol=1e-13, atol=1e-13)
+    o, kv, _ = oracle.linear_variant(q, k, v, cu, causal=True, normalize=False)
+    ro, rh = oracle.linear(q, k, v, None, cu)
+    assert _rel(o, ro) < 1e-13 and _rel(kv, rh) < 1e-13
+
+
+def test_bidirectional_is_order_free_and_reassociates():
+    """Bidirectional outputs do not depend on the order of the sequence's
+    tokens (permuting k and v together leaves every o_t unchanged), and they
+    equal the reassociated evaluation q_t (K^T V) / (q_t . K^T 1)."""
+    rng = np.random.default_rng(34)
+    q, k, v, cu = _positive_case(rng, [30], 2, 6, 4)
+    for norm in (True, False):
+        o, kv, z = oracle.linear_variant(q, k, v, cu, causal=False, normalize=norm)
+        perm = rng.permutation(30)
+        o2, _, _ = oracle.linear_variant(q, k[perm], v[perm], cu, causal=False, normalize=norm)
+        np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-12)
+        for h in range(2):
+            num = q[:, h] @ kv[0, h]
+            ref = num / (q[:, h] @ z[0, h])[:, None] if norm else num
+            np.testing.assert_allclose(o[:, h], ref, rtol=1e-12, atol=1e-12)
+    o, _, _ = oracle.linear_variant(q, k, v, cu, causal=True, normalize=True)
+    o2, _, _ = oracle.linear_variant(q, k[perm], v[perm], cu, causal=True, normalize=True)
+    assert _rel(o2, o) > 1e-3  # the causal form does depend on the order
+
+
 def test_decode_step_equals_one_prefill_token():
     rng = np.random.default_rng(12)
     B, H, dk, dv = 3, 2, 5, 4
