@@ -7,7 +7,9 @@ larger than L2 (4.35 GB), so no L2 flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --workload {gdn_t32768_h16, gdn_t131072_h32_single, gdn_t65536_h8, linear_b2_t4096_h8,
-                              decode_b128_h32, gdn_varlen_t131072_h32_block_adjacent, gdn_t131072_h4}
+                              decode_b128_h32, gdn_varlen_t131072_h32_block_adjacent, gdn_t131072_h4,
+                              linear_bidir_norm_b2_t4096_h8, linear_causal_norm_b2_t4096_h8,
+                              linear_bidir_norm_t131072_h32, linear_causal_norm_t131072_h32}
                                                    (the other workloads, one GPU)
 
 One JSON line is printed by rank 0.  Under torchrun each rank runs the same
@@ -415,6 +417,13 @@ def run_workload(args):
         elif name == "gdn_t16384_h4":  # the same length with few units
             lengths, Hh, kind = [16384], 4, "gdn"
             inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
+        elif name.startswith("linear_bidir_norm_") or name.startswith("linear_causal_norm_"):
+            # linear-attention variants: causal or bidirectional, normalised
+            lengths, Hh = ([4096, 4096], 8) if name.endswith("b2_t4096_h8") else ([131072], 32)
+            kind = "bidir_norm" if "bidir" in name else "causal_norm"
+            inp = gi.linear_inputs(lengths, Hh, D, D, "bf16", seed=0)
+            if Hh == 8:
+                flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
         elif name == "gdn_t131072_h4":  # one long sequence, few heads: the two-level state scan
             lengths, Hh, kind = [131072], 4, "gdn"
             inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
@@ -430,7 +439,15 @@ def run_workload(args):
         gdn_kind = kind.startswith("gdn")
         wsz = g.chunk_fwd_workspace_size(Tt, Hh, D, D, nn, delta_rule=gdn_kind)
         ws = torch.empty(max(wsz, 256), dtype=torch.uint8, device="cuda")
-        if gdn_kind:
+        if kind in ("bidir_norm", "causal_norm"):
+            causal = kind == "causal_norm"
+            ws = None
+
+            def run():
+                nonlocal ws
+                _, _, _, ws = g.linear_attn_variant(d["q"], d["k"], d["v"], d["cu_seqlens"], causal=causal,
+                                                    normalize=True, o=o, workspace=ws)
+        elif gdn_kind:
             band = kind == "gdn_block_adjacent"
 
             def run():
@@ -445,6 +462,10 @@ def run_workload(args):
             (2 if gdn_kind else 1) * nn * Hh * D * D * 4
         segs = g.two_level_segments(Tt, Hh, nn, delta_rule=gdn_kind)
         launches = 2 if segs < 2 else (7 if gdn_kind else 6)
+        if kind == "bidir_norm":  # plan, K^T V reduction, apply
+            bytes_per_call, launches, segs = 4 * Tt * Hh * D * 2, 3, 1
+        elif kind == "causal_norm":  # the causal prefill, a plan, key sums, prefix, normalise
+            bytes_per_call, launches = 4 * Tt * Hh * D * 2, launches + 4
         cfg = {"workload": name, "T": Tt, "H": Hh, "dk": D, "dv": D, "seq_lens": lengths,
                "two_level_segments": segs,
                "chunk": 64, "path": kernel_name(True, nn * Hh), "l2": ("L2 flushed (256 MB write) between timed calls"

@@ -55,6 +55,11 @@ lib.gdn_workspace_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
 lib.gdn_workspace_status.restype = _i
 lib.gdn_workspace_timeout_site.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
 lib.gdn_workspace_timeout_site.restype = _i
+lib.linear_attn_variant_workspace_size.argtypes = [_i64, _i, _i, _i, _i, _i, _i, _i]
+lib.linear_attn_variant_workspace_size.restype = _sz
+lib.linear_attn_variant_fwd.argtypes = [_vp, _vp, _vp, _ip, _i, _i64, _i, _i, _i, _i, _i, _i, _vp, _fp,
+                                        _fp, _vp, _sz, _vp]
+lib.linear_attn_variant_fwd.restype = _i
 lib.gdn_prefill_segments.argtypes = [_i64, _i, _i, _i, _i, _i, _i]
 lib.gdn_prefill_segments.restype = _i
 lib.gdn_set_wait_limit.argtypes = [_i]
@@ -272,3 +277,23 @@ def two_level_segments(T, H, n_seqs, dk=128, dv=128, dtype=torch.bfloat16, delta
     """Segments per sequence a prefill call of these sizes takes (1: one pass)."""
     io = GDN_BF16 if dtype == torch.bfloat16 else GDN_FP32
     return int(lib.gdn_prefill_segments(T, H, dk, dv, n_seqs, io, int(bool(delta_rule))))
+
+
+def linear_attn_variant(q, k, v, cu_seqlens=None, *, causal=True, normalize=False, o=None,
+                        output_kv=False, output_z=False, workspace=None, stream=None):
+    """Linear attention, causal or bidirectional, optionally normalised, through
+    the C ABI; returns (o, kv, z, workspace) with kv = K^T V [N,H,dk,dv] and
+    z = summed keys [N,H,dk] (fp32, None unless asked for)."""
+    _check_inputs(q, k, v, None, None, None, cu_seqlens)
+    T, H, dk, dv, n = _prefill_shapes(q, k, v, cu_seqlens)
+    o, _ = _outputs(q, v, n, H, dk, dv, o, None, False)
+    kv = torch.empty(n, H, dk, dv, dtype=torch.float32, device=q.device) if output_kv else None
+    z = torch.empty(n, H, dk, dtype=torch.float32, device=q.device) if output_z else None
+    need = lib.linear_attn_variant_workspace_size(T, H, dk, dv, n, _io(q), int(bool(causal)),
+                                                  int(bool(normalize)))
+    ws = _alloc_ws(need, q.device, workspace)
+    rc = lib.linear_attn_variant_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), n, T, H, dk, dv,
+                                     _io(q), int(bool(causal)), int(bool(normalize)), _ptr(o),
+                                     _ptr(kv), _ptr(z), _ptr(ws), ws.numel(), _stream(q, stream))
+    _check(rc, "linear_attn_variant_fwd")
+    return o, kv, z, ws

@@ -238,6 +238,48 @@ gdn_status linear_attn_fwd(const void* q, const void* k, const void* v, const fl
     return prefill(a, ws_bytes, (cudaStream_t)stream);
 }
 
+size_t linear_attn_variant_workspace_size(int64_t T, int H, int dk, int dv, int n_seqs, gdn_dtype io,
+                                          int causal, int normalize) {
+    (void)normalize;
+    if (!sizes_ok(T, H, dk, dv, n_seqs) || io != GDN_BF16 || dk != 128 || dv != 128) return 0;
+    const size_t extra = linear_variant_extra_bytes(T, H, n_seqs, causal != 0);
+    if (!causal) return align256(plan_bytes(n_seqs)) + extra;
+    const size_t num = (linear_attn_fwd_workspace_size(T, H, dk, dv, n_seqs, io) + 1023) & ~(size_t)1023;
+    return num + align256(plan_bytes(n_seqs)) + extra;
+}
+
+gdn_status linear_attn_variant_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                                   int n_seqs, int64_t T_total, int H, int dk, int dv, gdn_dtype io_dtype,
+                                   int causal, int normalize, void* o, float* kv, float* z, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+    PrefillArgs a = make_args(q, k, v, nullptr, nullptr, nullptr, cu_seqlens, n_seqs, T_total, H, dk, dv,
+                              io_dtype, false, o, kv, workspace);
+    const size_t need = linear_attn_variant_workspace_size(T_total, H, dk, dv, n_seqs, io_dtype, causal, normalize);
+    gdn_status s = check_prefill(a, ws_bytes, need, true);
+    if (s != GDN_OK) return s;
+    if (!linear_variant_shape_ok(a) || need == 0) return GDN_ERR_UNSUPPORTED;
+    if (!aligned(z, 16)) return GDN_ERR_ALIGN;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int wl = g_wait_limit.load();
+    if (!causal) {
+        char* plan = a.ws;
+        char* extra = a.ws + align256(plan_bytes(n_seqs));
+        cudaError_t e = launch_plan(cu_seqlens, n_seqs, T_total, wl, plan, st);
+        if (e == cudaSuccess) e = launch_linear_bidirectional(a, plan, extra, normalize != 0, kv, z, st);
+        return cuda_status(e);
+    }
+    // causal: the numerator is the causal linear attention (h_T = K^T V when asked)
+    const size_t num = (linear_attn_fwd_workspace_size(T_total, H, dk, dv, n_seqs, io_dtype) + 1023) & ~(size_t)1023;
+    s = prefill(a, num, st);
+    if (s != GDN_OK) return s;
+    if (!normalize && z == nullptr) return GDN_OK;
+    char* plan = a.ws + num;
+    char* extra = plan + align256(plan_bytes(n_seqs));
+    cudaError_t e = launch_plan(cu_seqlens, n_seqs, T_total, wl, plan, st, reinterpret_cast<const int*>(a.ws));
+    if (e == cudaSuccess) e = launch_linear_causal_normaliser(a, plan, extra, normalize != 0, z, st);
+    return cuda_status(e);
+}
+
 gdn_status gdn_chunk_fwd_staged(const void* q, const void* k, const void* v,
                                 const float* log_alpha, const float* beta, const float* h0,
                                 const int32_t* cu_seqlens, int n_seqs, int64_t T_total, int H,

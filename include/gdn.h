@@ -168,6 +168,35 @@ GDN_API gdn_status linear_attn_fwd(const void *q, const void *k, const void *v, 
                            void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Linear attention, causal or bidirectional, with or without the normaliser
+ * (bf16 q, k, v, o; dk = dv = 128; other combinations return
+ * GDN_ERR_UNSUPPORTED):
+ *     o_t = sum_s (q_t . k_s) v_s  [ / sum_s (q_t . k_s) ],
+ * s over all tokens of t's sequence (causal = 0) or over s <= t (causal = 1).
+ * The bidirectional, normalised form is the listing of "За пределами
+ * self-attention…" (section "Линейное внимание…": K^T V and the summed keys
+ * first, then q_t times each); the bidirectional mode and the causal
+ * restriction are the two modes of the ai-vestnik.ru item on linear
+ * attention (HSE / VK students).  Feature maps (elu + 1 on the page) are the
+ * caller's: q and k are used as given; no epsilon is added to the normaliser,
+ * so normalised calls need q_t . sum k_s != 0 (positive features give that).
+ * No initial state.  Optional fp32 outputs (NULL to skip, 16-byte aligned):
+ * kv [n_seqs][H][dk][dv] = sum_t k_t v_t^T over each sequence (h = S^T of the
+ * final state), z [n_seqs][H][dk] = sum_t k_t.  Bidirectional calls run a
+ * tcgen05 reduction of K^T V over groups of chunks and a tcgen05 apply pass;
+ * causal calls run the causal prefill of linear_attn_fwd for the numerator
+ * and, when normalised, a key-prefix pass that divides o.  Workspace: the
+ * query below; status word at its offset 0, as for the other calls.
+ */
+GDN_API size_t linear_attn_variant_workspace_size(int64_t T_total, int H, int dk, int dv, int n_seqs,
+                                          gdn_dtype io_dtype, int causal, int normalize);
+GDN_API gdn_status linear_attn_variant_fwd(const void *q, const void *k, const void *v,
+                                   const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
+                                   int dk, int dv, gdn_dtype io_dtype, int causal, int normalize,
+                                   void *o, float *kv, float *z, void *workspace, size_t ws_bytes,
+                                   void *stream);
+
+/*
  * One decode token of the gated delta rule for B sequences x H heads, the
  * state updated in place: S <- a S + b (v - a S k) k^T, o = S q (the same
  * rule as above for a single t; O(1) state per step as in "Как ускорить LLM

@@ -259,3 +259,22 @@ def linear_variant(q, k, v, cu_seqlens=None, causal=True, normalize=False):
             kv[s, h] = K.T @ V
             z[s, h] = K.sum(axis=0)
     return o, kv, z
+
+
+def linear_sums(k, v, cu_seqlens=None):
+    """Per sequence and head, kv = K^T V and z = K^T 1 (fp64): the aggregates
+    the bidirectional form reassociates through (same page and listing as
+    linear_variant), without the T x T weights, for long inputs."""
+    k, v = _f64(k), _f64(v)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    N = len(cu) - 1
+    kv = np.zeros((N, H, dk, dv))
+    z = np.zeros((N, H, dk))
+    for s in range(N):
+        a, e = int(cu[s]), int(cu[s + 1])
+        for h in range(H):
+            kv[s, h] = k[a:e, h].T @ v[a:e, h]
+            z[s, h] = k[a:e, h].sum(axis=0)
+    return kv, z

@@ -390,6 +390,78 @@ def test_two_level_scan_default_t131072_h4(g, monkeypatch):
     check_chains(inp, o, hT, [(0, 1), (0, 3)], TOL["bf16"])
 
 
+# ------------------------------------------------------------------ linear-attention variants
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("normalize", [True, False])
+def test_linear_variants_against_oracle(g, causal, normalize):
+    """Causal or bidirectional, normalised or not, on ragged packed sequences
+    (a one-token and an empty sequence included): every output, K^T V and the
+    summed keys against the oracle's quadratic form."""
+    lengths = [1, 100, 0, 257, 64, 700]
+    inp = gi.linear_inputs(lengths, 4, 128, 128, "bf16", seed=51)
+    d = dev(inp)
+    o, kv, z, ws = g.linear_attn_variant(d["q"], d["k"], d["v"], d["cu_seqlens"], causal=causal,
+                                         normalize=normalize, output_kv=True, output_z=True)
+    assert g.workspace_status(ws) == 0
+    ro, rkv, rz = oracle.linear_variant(inp["q"], inp["k"], inp["v"], inp["cu_seqlens"], causal=causal,
+                                        normalize=normalize)
+    assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
+    assert rel(kv, rkv) <= TOL["bf16"], rel(kv, rkv)
+    assert rel(z, rz) <= TOL["bf16"], rel(z, rz)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("normalize", [True, False])
+def test_linear_variants_b2_t4096_h8(g, causal, normalize):
+    """The linear-attention workload's shapes (2 x 4096 tokens, H = 8): every
+    output against the oracle."""
+    inp = gi.linear_inputs([4096, 4096], 8, 128, 128, "bf16", seed=0)
+    d = dev(inp)
+    o, _, _, ws = g.linear_attn_variant(d["q"], d["k"], d["v"], d["cu_seqlens"], causal=causal,
+                                        normalize=normalize)
+    assert g.workspace_status(ws) == 0
+    ro, _, _ = oracle.linear_variant(inp["q"], inp["k"], inp["v"], inp["cu_seqlens"], causal=causal,
+                                     normalize=normalize)
+    assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
+
+
+def test_linear_bidirectional_normalised_t131072_h32(g):
+    """One 131072-token sequence, H = 32, bidirectional and normalised: K^T V
+    and the summed keys of every head against the oracle's sums, and sampled
+    tokens of every head against q_t (K^T V) / (q_t . z) from those sums (the
+    reassociation the oracle pins against its quadratic form)."""
+    inp = gi.linear_inputs([131072], 32, 128, 128, "bf16", seed=1)
+    d = dev(inp)
+    o, kv, z, ws = g.linear_attn_variant(d["q"], d["k"], d["v"], None, causal=False, normalize=True,
+                                         output_kv=True, output_z=True)
+    assert g.workspace_status(ws) == 0
+    rkv, rz = oracle.linear_sums(inp["k"], inp["v"])
+    assert rel(kv, rkv) <= TOL["bf16"] and rel(z, rz) <= TOL["bf16"]
+    ts = torch.randint(0, 131072, (64,), generator=torch.Generator().manual_seed(5))
+    qs = inp["q"][ts].double().numpy()  # [64, H, dk]
+    ref = np.einsum("thi,hij->thj", qs, rkv[0]) / np.einsum("thi,hi->th", qs, rz[0])[..., None]
+    assert rel(o[ts.cuda()], ref) <= TOL["bf16"]
+
+
+def test_linear_bidirectional_forced_timeout_then_recovery(g):
+    inp = gi.linear_inputs([300, 500], 4, 128, 128, "bf16", seed=52)
+    d = dev(inp)
+    old = g.set_wait_limit(0)
+    try:
+        _, _, _, ws = g.linear_attn_variant(d["q"], d["k"], d["v"], d["cu_seqlens"], causal=False,
+                                            normalize=True)
+        assert g.workspace_status(ws) in (0, -9)
+    finally:
+        g.set_wait_limit(old)
+    o, _, _, _ = g.linear_attn_variant(d["q"], d["k"], d["v"], d["cu_seqlens"], causal=False,
+                                       normalize=True, workspace=ws)
+    assert g.workspace_status(ws) == 0
+    ro, _, _ = oracle.linear_variant(inp["q"], inp["k"], inp["v"], inp["cu_seqlens"], causal=False,
+                                     normalize=True)
+    assert rel(o, ro) <= TOL["bf16"]
+
+
 # ------------------------------------------------------------------ failure detection
 
 @pytest.mark.parametrize("kernel", KERNELS)

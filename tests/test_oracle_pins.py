@@ -338,6 +338,9 @@ def test_linear_variants_brute_force():
                     np.testing.assert_allclose(z[sq, h], k[a:e, h].sum(axis=0), rtol=1e-13)
                     ref_kv = sum(np.outer(k[u, h], v[u, h]) for u in range(a, e)) if e > a else 0.0
                     np.testing.assert_allclose(kv[sq, h], ref_kv, rtol=1e-13, atol=1e-13)
+            kv2, z2 = oracle.linear_sums(k, v, cu)
+            np.testing.assert_allclose(kv2, kv, rtol=1e-13, atol=1e-13)
+            np.testing.assert_allclose(z2, z, rtol=1e-13, atol=1e-13)
 
 
 def test_normalised_weights_sum_to_one():
