@@ -9,7 +9,8 @@ larger than L2 (4.35 GB), so no L2 flush is needed between steps.
   python bench.py --workload {gdn_t32768_h16, gdn_t131072_h32_single, gdn_t65536_h8, linear_b2_t4096_h8,
                               decode_b128_h32, gdn_varlen_t131072_h32_block_adjacent, gdn_t131072_h4,
                               linear_bidir_norm_b2_t4096_h8, linear_causal_norm_b2_t4096_h8,
-                              linear_bidir_norm_t131072_h32, linear_causal_norm_t131072_h32}
+                              linear_bidir_norm_t131072_h32, linear_causal_norm_t131072_h32,
+                              linear_bidir_norm_t32768_h32 (any _t<T>_h<H>)}
                                                    (the other workloads, one GPU)
 
 One JSON line is printed by rank 0.  Under torchrun each rank runs the same
@@ -419,7 +420,11 @@ def run_workload(args):
             inp = gi.gdn_inputs(lengths, Hh, D, D, "bf16", h0_std=0.01, seed=0)
         elif name.startswith("linear_bidir_norm_") or name.startswith("linear_causal_norm_"):
             # linear-attention variants: causal or bidirectional, normalised
-            lengths, Hh = ([4096, 4096], 8) if name.endswith("b2_t4096_h8") else ([131072], 32)
+            if name.endswith("b2_t4096_h8"):
+                lengths, Hh = [4096, 4096], 8
+            else:  # ..._t<T>_h<H>: one sequence
+                tt, hh = name.rsplit("_", 2)[-2:]
+                lengths, Hh = [int(tt[1:])], int(hh[1:])
             kind = "bidir_norm" if "bidir" in name else "causal_norm"
             inp = gi.linear_inputs(lengths, Hh, D, D, "bf16", seed=0)
             if Hh == 8:
