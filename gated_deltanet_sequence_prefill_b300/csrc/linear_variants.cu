@@ -439,22 +439,58 @@ chunk_key_sum_kernel(const __nv_bfloat16* __restrict__ k, int H, const char* __r
 }
 
 // Exclusive prefix of the chunk key sums over each sequence's chunks, and the
-// sequence's total (the summed keys z, when asked for).
-__global__ void __launch_bounds__(kThreads)
+// sequence's total (the summed keys z, when asked for).  One block per
+// (sequence, head, 16 features): each of its 256 threads takes a contiguous
+// run of the sequence's chunks for those 16 features, the runs' totals are
+// scanned in shared memory, and each thread then writes its run's prefixes.
+constexpr int kPrefixThreads = 256, kPrefixFeat = 16;
+__global__ void __launch_bounds__(kPrefixThreads)
 key_prefix_kernel(int H, const char* __restrict__ ws, const float* __restrict__ ks,
                   float* __restrict__ zstart, float* __restrict__ z) {
+    __shared__ float part[kPrefixThreads][kPrefixFeat + 1];
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
     if (hdr->status != GDN_OK) return;
     PlanLayout L(hdr->n_seqs);
     const int* chunk_off = reinterpret_cast<const int*>(ws + L.chunk_off);
-    const int seq = blockIdx.x, head = blockIdx.y, i = threadIdx.x;
-    float run = 0.f;
-    for (int c = chunk_off[seq]; c < chunk_off[seq + 1]; ++c) {
-        const size_t at = ((size_t)c * H + head) * kD + i;
-        zstart[at] = run;
-        run += ks[at];
+    const int seq = blockIdx.x, head = blockIdx.y, f0 = blockIdx.z * kPrefixFeat, tid = threadIdx.x;
+    const int c0 = chunk_off[seq], nch = chunk_off[seq + 1] - c0;
+    const int per = (nch + kPrefixThreads - 1) / kPrefixThreads;
+    const int a = c0 + min(nch, tid * per), e = c0 + min(nch, (tid + 1) * per);
+    float run[kPrefixFeat];
+#pragma unroll
+    for (int x = 0; x < kPrefixFeat; ++x) run[x] = 0.f;
+    for (int c = a; c < e; ++c) {
+        const float* src = ks + ((size_t)c * H + head) * kD + f0;
+#pragma unroll
+        for (int x = 0; x < kPrefixFeat; ++x) run[x] += src[x];
     }
-    if (z) z[((size_t)seq * H + head) * kD + i] = run;
+#pragma unroll
+    for (int x = 0; x < kPrefixFeat; ++x) part[tid][x] = run[x];
+    __syncthreads();
+    // inclusive scan of the runs' totals, per feature (Hillis-Steele over 256 entries)
+    for (int off = 1; off < kPrefixThreads; off <<= 1) {
+        float add[kPrefixFeat];
+#pragma unroll
+        for (int x = 0; x < kPrefixFeat; ++x) add[x] = tid >= off ? part[tid - off][x] : 0.f;
+        __syncthreads();
+#pragma unroll
+        for (int x = 0; x < kPrefixFeat; ++x) part[tid][x] += add[x];
+        __syncthreads();
+    }
+#pragma unroll
+    for (int x = 0; x < kPrefixFeat; ++x) run[x] = tid > 0 ? part[tid - 1][x] : 0.f;  // before this run
+    for (int c = a; c < e; ++c) {
+        const size_t at = ((size_t)c * H + head) * kD + f0;
+#pragma unroll
+        for (int x = 0; x < kPrefixFeat; ++x) {
+            zstart[at + x] = run[x];
+            run[x] += ks[at + x];
+        }
+    }
+    if (z && tid == kPrefixThreads - 1) {
+#pragma unroll
+        for (int x = 0; x < kPrefixFeat; ++x) z[((size_t)seq * H + head) * kD + f0 + x] = part[tid][x];
+    }
 }
 
 // o_t /= q_t . (z_start + sum of k_s over s <= t in the chunk), per chunk.
@@ -558,7 +594,8 @@ cudaError_t launch_linear_causal_normaliser(const PrefillArgs& a, char* plan_ws,
     chunk_key_sum_kernel<<<dim3((unsigned)nch, a.H), kThreads, 0, st>>>((const __nv_bfloat16*)a.k, a.H, plan_ws, ks);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && a.n_seqs > 0) {
-        key_prefix_kernel<<<dim3((unsigned)a.n_seqs, a.H), kThreads, 0, st>>>(a.H, plan_ws, ks, zstart, z_out);
+        key_prefix_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / kPrefixFeat), kPrefixThreads, 0, st>>>(
+            a.H, plan_ws, ks, zstart, z_out);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess && divide) {
