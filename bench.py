@@ -43,6 +43,15 @@ def kernel_name(fused, units=None):
     return "fused_single_sm" if os.environ.get("GDN_PREFILL_PAIR", "") == "0" else "fused_pair"
 
 
+def linear_grouped():
+    """Whether linear_attn_fwd (bf16, d = 128) takes the grouped causal path
+    (the library's own rule: yes unless GDN_LINEAR_PATH=cluster,
+    GDN_PREFILL_PAIR=0 or GDN_TWO_LEVEL picks the fused kernels)."""
+    if os.environ.get("GDN_LINEAR_PATH", "") == "cluster" or os.environ.get("GDN_PREFILL_PAIR", "") == "0":
+        return False
+    return os.environ.get("GDN_TWO_LEVEL", "") == ""
+
+
 def source_digest(kernel):
     import hashlib
     path = os.path.join(ROOT, "gated_deltanet_sequence_prefill_b300", "csrc", KERNEL_SRC.get(kernel, ""))
@@ -467,13 +476,17 @@ def run_workload(args):
             (2 if gdn_kind else 1) * nn * Hh * D * D * 4
         segs = g.two_level_segments(Tt, Hh, nn, delta_rule=gdn_kind)
         launches = 2 if segs < 2 else (7 if gdn_kind else 6)
+        path = kernel_name(True, nn * Hh)
         if kind == "bidir_norm":  # plan, K^T V reduction, apply
-            bytes_per_call, launches, segs = 4 * Tt * Hh * D * 2, 3, 1
-        elif kind == "causal_norm":  # the causal prefill, a plan, key sums, prefix, normalise
-            bytes_per_call, launches = 4 * Tt * Hh * D * 2, launches + 4
+            bytes_per_call, launches, segs, path = 4 * Tt * Hh * D * 2, 3, 1, "linear_bidirectional"
+        elif kind == "causal_norm" or (kind == "linear" and linear_grouped()):
+            # plan, group plan, half-group K^T V sums, prefix over the groups, group apply
+            launches, segs, path = 5, 1, "linear_grouped"
+            if kind == "causal_norm":
+                bytes_per_call = 4 * Tt * Hh * D * 2
         cfg = {"workload": name, "T": Tt, "H": Hh, "dk": D, "dv": D, "seq_lens": lengths,
                "two_level_segments": segs,
-               "chunk": 64, "path": kernel_name(True, nn * Hh), "l2": ("L2 flushed (256 MB write) between timed calls"
+               "chunk": 64, "path": path, "l2": ("L2 flushed (256 MB write) between timed calls"
                                    if flush is not None else "inputs larger than L2, no flush")}
     for _ in range(args.warmup):
         run()

@@ -2,6 +2,7 @@
 // host-side argument checks, workspace carving and kernel launches.
 #include <cuda_runtime.h>
 #include <stdlib.h>
+#include <string.h>
 #include <stdint.h>
 
 #include <atomic>
@@ -116,7 +117,33 @@ bool use_pair(const PrefillArgs& a) {
     return !(e != nullptr && e[0] == '0');
 }
 
+// Causal linear attention (bf16, dk = dv = 128) runs through groups of chunks
+// (linear_variants.cu) unless the environment picks another path:
+// GDN_LINEAR_PATH=cluster or GDN_PREFILL_PAIR=0 (the fused prefill kernels)
+// or GDN_TWO_LEVEL (the two-level scan over the cluster kernel).
+bool use_grouped_linear(const PrefillArgs& a) {
+    if (a.delta_rule || a.io != GDN_BF16 || a.dk != 128 || a.dv != 128) return false;
+    const char* e = getenv("GDN_LINEAR_PATH");
+    if (e != nullptr && strcmp(e, "cluster") == 0) return false;
+    const char* p = getenv("GDN_PREFILL_PAIR");
+    if (p != nullptr && p[0] == '0') return false;
+    const char* t = getenv("GDN_TWO_LEVEL");
+    return !(t != nullptr && t[0] != '\0');
+}
+
+size_t grouped_linear_bytes(int64_t T, int H, int n_seqs) {
+    return align256(plan_bytes(n_seqs)) + linear_grouped_extra_bytes(T, H, n_seqs);
+}
+
 gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
+    if (use_grouped_linear(a)) {
+        gdn_status s = check_prefill(a, ws_bytes, grouped_linear_bytes(a.T_total, a.H, a.n_seqs), true);
+        if (s != GDN_OK) return s;
+        cudaError_t e = launch_plan(a.cu_seqlens, a.n_seqs, a.T_total, g_wait_limit.load(), a.ws, st);
+        if (e == cudaSuccess)
+            e = launch_linear_grouped(a, a.ws, a.ws + align256(plan_bytes(a.n_seqs)), false, a.h_T, nullptr, st);
+        return cuda_status(e);
+    }
     const bool pair = use_pair(a);
     if (pair) {
         const int G = two_level_segments(a);
@@ -193,6 +220,7 @@ size_t linear_attn_fwd_workspace_size(int64_t T, int H, int dk, int dv, int n_se
     if (!sizes_ok(T, H, dk, dv, n_seqs) || (io != GDN_BF16 && io != GDN_FP32)) return 0;
     PrefillArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, n_seqs,
                               T, H, dk, dv, io, false, nullptr, nullptr, nullptr);
+    if (use_grouped_linear(a)) return grouped_linear_bytes(T, H, n_seqs);
     if (pair_shape_ok(a)) {
         const int G = two_level_segments(a);
         return G >= 2 ? two_level_workspace_bytes(n_seqs, H, G) : pair_workspace_bytes(n_seqs, H);
@@ -242,10 +270,7 @@ size_t linear_attn_variant_workspace_size(int64_t T, int H, int dk, int dv, int 
                                           int causal, int normalize) {
     (void)normalize;
     if (!sizes_ok(T, H, dk, dv, n_seqs) || io != GDN_BF16 || dk != 128 || dv != 128) return 0;
-    const size_t extra = linear_variant_extra_bytes(T, H, n_seqs, causal != 0);
-    if (!causal) return align256(plan_bytes(n_seqs)) + extra;
-    const size_t num = (linear_attn_fwd_workspace_size(T, H, dk, dv, n_seqs, io) + 1023) & ~(size_t)1023;
-    return num + align256(plan_bytes(n_seqs)) + extra;
+    return align256(plan_bytes(n_seqs)) + linear_variant_extra_bytes(T, H, n_seqs, causal != 0);
 }
 
 gdn_status linear_attn_variant_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
@@ -261,22 +286,12 @@ gdn_status linear_attn_variant_fwd(const void* q, const void* k, const void* v, 
     if (!aligned(z, 16)) return GDN_ERR_ALIGN;
     cudaStream_t st = (cudaStream_t)stream;
     const int wl = g_wait_limit.load();
-    if (!causal) {
-        char* plan = a.ws;
-        char* extra = a.ws + align256(plan_bytes(n_seqs));
-        cudaError_t e = launch_plan(cu_seqlens, n_seqs, T_total, wl, plan, st);
-        if (e == cudaSuccess) e = launch_linear_bidirectional(a, plan, extra, normalize != 0, kv, z, st);
-        return cuda_status(e);
-    }
-    // causal: the numerator is the causal linear attention (h_T = K^T V when asked)
-    const size_t num = (linear_attn_fwd_workspace_size(T_total, H, dk, dv, n_seqs, io_dtype) + 1023) & ~(size_t)1023;
-    s = prefill(a, num, st);
-    if (s != GDN_OK) return s;
-    if (!normalize && z == nullptr) return GDN_OK;
-    char* plan = a.ws + num;
-    char* extra = plan + align256(plan_bytes(n_seqs));
-    cudaError_t e = launch_plan(cu_seqlens, n_seqs, T_total, wl, plan, st, reinterpret_cast<const int*>(a.ws));
-    if (e == cudaSuccess) e = launch_linear_causal_normaliser(a, plan, extra, normalize != 0, z, st);
+    char* plan = a.ws;
+    char* extra = a.ws + align256(plan_bytes(n_seqs));
+    cudaError_t e = launch_plan(cu_seqlens, n_seqs, T_total, wl, plan, st);
+    if (e == cudaSuccess)
+        e = causal ? launch_linear_grouped(a, plan, extra, normalize != 0, kv, z, st)
+                   : launch_linear_bidirectional(a, plan, extra, normalize != 0, kv, z, st);
     return cuda_status(e);
 }
 

@@ -82,14 +82,17 @@ int two_level_segments(const PrefillArgs& a);
 size_t two_level_workspace_bytes(int n_seqs, int H, int G);
 cudaError_t launch_two_level(const PrefillArgs& a, int G, int wait_limit, cudaStream_t st);
 
-// Linear-attention variants (bf16, dk = dv = 128): bidirectional via K^T V,
-// and the causal normaliser beside the causal prefill.  plan_ws holds a plan
-// of the call's sequences; extra holds linear_variant_extra_bytes().
+// Linear attention (bf16, dk = dv = 128) without the cluster kernel:
+// bidirectional via K^T V, and causal through groups of chunks (normalised or
+// not).  plan_ws holds a plan of the call's sequences; extra holds
+// linear_variant_extra_bytes() (bidirectional) or
+// linear_grouped_extra_bytes() (causal).
 bool linear_variant_shape_ok(const PrefillArgs& a);
 size_t linear_variant_extra_bytes(int64_t T, int H, int n_seqs, bool causal);
 cudaError_t launch_linear_bidirectional(const PrefillArgs& a, char* plan_ws, char* extra, bool normalize,
                                         float* kv_out, float* z_out, cudaStream_t st);
-cudaError_t launch_linear_causal_normaliser(const PrefillArgs& a, char* plan_ws, char* extra, bool divide,
-                                            float* z_out, cudaStream_t st);
+size_t linear_grouped_extra_bytes(int64_t T, int H, int n_seqs);
+cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* extra, bool normalize, float* h_T,
+                                  float* z_T, cudaStream_t st);
 
 }  // namespace gdn

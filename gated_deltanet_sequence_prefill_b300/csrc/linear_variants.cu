@@ -14,10 +14,11 @@
 // (tcgen05; K^T V and z rounded once to bf16 as the B operand, z as an extra
 // column so q . z comes out of the same MMA), divides by q . z when
 // normalised, and stores o with TMA.
-// Causal normalised: the numerator is the causal linear attention of the
-// library's prefill; the normaliser q_t . (sum of k_s, s <= t) comes from
-// per-chunk key sums, their prefix over the chunks of each sequence, and a
-// per-chunk pass that divides o.
+// Causal (normalised or not): the sequences are cut into groups of chunks; the
+// groups' K^T V and key sums give every group's starting state and key sum by
+// a prefix, and every group then runs its chunks from there, all groups side
+// by side (the causal normaliser q_t . (sum of k_s, s <= t) comes out of the
+// same pass).
 #include <cuda_runtime.h>
 
 #include <cuda.h>
@@ -34,7 +35,6 @@ bool encode_token_map(CUtensorMap* m, const void* ptr, int64_t T, int H);
 namespace linvar {
 
 constexpr int kD = 128;
-constexpr int kThreads = 128;  // the causal normaliser's kernels
 constexpr int kMinGroup = 4;   // chunks per reduce / apply CTA, at least
 
 struct ChunkRef {
@@ -49,8 +49,8 @@ __device__ __forceinline__ ChunkRef chunk_ref(const int* cu, const int* chunk_of
 }
 
 // Bounded wait by one thread.  A wait that runs out records GDN_ERR_TIMEOUT
-// (and the site) in the status word and sets the CTA's abort flag; every role
-// reads the flag after its group synchronises, so each group stops together.
+// (and the site) in the status word and sets the CTA's abort flag; a wait
+// that finds the flag set returns false at once.
 __device__ __noinline__ bool lv_wait(uint32_t bar, uint32_t parity, char* ws, volatile int* abort_flag, int site) {
     if (*abort_flag) return false;
     if (tc::mbar_try_wait(bar, parity)) return true;
@@ -60,6 +60,48 @@ __device__ __noinline__ bool lv_wait(uint32_t bar, uint32_t parity, char* ws, vo
     atomicCAS(&h->timeout_site, 0, site);
     *abort_flag = 1;
     return false;
+}
+// The same wait taken once for a whole warp (lane 0 waits) or a whole
+// 128-thread group (its leader waits), the outcome shared by all of them, so
+// that no member leaves a loop the others stay in.  The warp form reads the
+// abort flag after the warp has converged, one load of one address for all
+// 32 lanes (a shuffle of lane 0's result instead made the MMA warps of these
+// kernels measurably slower); the group form reduces the leader's result over
+// the group's named barrier.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, char* ws, volatile int* abort_flag, int site) {
+    if ((threadIdx.x & 31) == 0) lv_wait(bar, parity, ws, abort_flag, site);
+    __syncwarp();
+    return *abort_flag == 0;
+}
+__device__ __forceinline__ bool group_wait(bool leader, int bar_id, uint32_t bar, uint32_t parity, char* ws,
+                                           volatile int* abort_flag, int site) {
+    bool ok = true;
+    if (leader) ok = lv_wait(bar, parity, ws, abort_flag, site);
+    return tc::named_bar_and(bar_id, 128, ok);
+}
+
+// Sum of column f (0..127) of a 64-row bf16 k tile in two SW128 boxes, rows
+// 0..n-1 (the key sums; four running sums for a short dependent chain).
+__device__ __forceinline__ float key_column_sum(uint32_t k0, int f, int n) {
+    const uint32_t col = k0 + (uint32_t)(f >> 6) * 8192 + (uint32_t)((f & 7) * 2);
+    const uint32_t c16 = (uint32_t)((f & 63) >> 3);
+    auto at = [&](int t) {
+        uint16_t h;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h)
+                     : "r"(col + (uint32_t)t * 128 + (((c16 ^ (uint32_t)t) & 7u) << 4)));
+        return __bfloat162float(__ushort_as_bfloat16(h));
+    };
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int t = 0;
+#pragma unroll 4
+    for (; t + 4 <= n; t += 4) {
+        a0 += at(t);
+        a1 += at(t + 1);
+        a2 += at(t + 2);
+        a3 += at(t + 3);
+    }
+    for (; t < n; ++t) a0 += at(t);
+    return (a0 + a1) + (a2 + a3);
 }
 
 constexpr int kLvThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 4..7 the 128-thread worker group
@@ -75,9 +117,32 @@ enum { R_FULL = 0, R_READY = 3, R_EMPTY = 6, R_RUNDONE = 9, R_TFREE = 10, R_FIN 
 constexpr uint32_t kRSmem = kRBarOff + 128 + 1024;
 constexpr uint32_t kIdKV = tc::idesc_bf16(128, 128, true, true);  // A = k^T, B = v, both MN-major
 
+// Sequence and chunk range of group g when every sequence is cut into groups
+// of `group` consecutive chunks (group_off[s] = first group of sequence s).
+__device__ __forceinline__ void group_range(const int* group_off, const int* chunk_off, int n_seqs, int group,
+                                            int g, int& seq, int& c0, int& nc) {
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (group_off[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    seq = lo;
+    c0 = chunk_off[seq] + (g - group_off[seq]) * group;
+    nc = max(0, min(chunk_off[seq + 1], c0 + group) - c0);
+}
+
+// GROUPED = false: bidirectional sums; CTA (x, head) takes the global chunks
+//   [x group, (x + 1) group) and adds each sequence's part of K^T V and of the
+//   key sums to kv[seq][head], z[seq][head].
+// GROUPED = true: the causal path's group sums in two halves; CTA (2 g + p,
+//   head) takes half p of group g (group_off, the group size in
+//   group_off[n_seqs + 1]) and writes its K^T V and key sums to
+//   kv[2 g + p][head], z[2 g + p][head].
+template <bool GROUPED>
 __global__ void __launch_bounds__(kLvThreads, 1)
 kv_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, int H,
-                 int group, char* __restrict__ ws, float* __restrict__ kv, float* __restrict__ z) {
+                 int group, char* __restrict__ ws, const int* __restrict__ group_off, float* __restrict__ kv,
+                 float* __restrict__ z) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -86,12 +151,30 @@ kv_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
     if (hdr->status != GDN_OK) return;
     const int total = hdr->total_chunks, n_seqs = hdr->n_seqs;
-    const int g0 = blockIdx.x * group, head = blockIdx.y;
-    if (g0 >= total) return;
-    const int nc = min(total, g0 + group) - g0;
+    const int head = blockIdx.y;
     PlanLayout L(n_seqs);
     const int* cu = reinterpret_cast<const int*>(ws + L.cu);
     const int* chunk_off = reinterpret_cast<const int*>(ws + L.chunk_off);
+    int g0, nc, gseq = 0;
+    if (GROUPED) {  // CTA x = 2 g + part takes the first or the second half of group g
+        const int gg = blockIdx.x >> 1, part = blockIdx.x & 1;
+        if (gg >= group_off[n_seqs]) return;
+        int c0g, ncg;
+        group_range(group_off, chunk_off, n_seqs, group_off[n_seqs + 1], gg, gseq, c0g, ncg);
+        const int first = (ncg + 1) >> 1;
+        g0 = part ? c0g + first : c0g;
+        nc = part ? ncg - first : first;
+        if (nc == 0) {  // an empty half: its partial sums are zero
+            float* dst = kv + ((size_t)blockIdx.x * H + head) * kD * kD;
+            for (int x = threadIdx.x; x < kD * kD; x += blockDim.x) dst[x] = 0.f;
+            if (threadIdx.x < kD) z[((size_t)blockIdx.x * H + head) * kD + threadIdx.x] = 0.f;
+            return;
+        }
+    } else {
+        g0 = blockIdx.x * group;
+        if (g0 >= total) return;
+        nc = min(total, g0 + group) - g0;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     auto bar = [&](int i) { return sbase + kRBarOff + 8u * (uint32_t)i; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + kRBarOff + 96);
@@ -135,31 +218,27 @@ kv_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     } else if (warp == 1) {
         // ---- MMA: D (TMEM, 128 x 128 fp32) += k^T v per chunk; one run per sequence
         int run_seq = -1, runs = 0;
-        bool fresh = true;
-        for (int i = 0; i < nc; ++i) {
+        bool fresh = true, ok = true;
+        for (int i = 0; i < nc && ok; ++i) {
             const int s = i % kRStages;
             const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, g0 + i);
             if (r.seq != run_seq) {
                 if (run_seq >= 0) {
                     tc::commit_e(bar(R_RUNDONE));  // the run's MMAs are done: the workers may read D
-                    if (lane == 0) lv_wait(bar(R_TFREE), (runs - 1) & 1, ws, abort_flag, 4101);
-                    __syncwarp();
-                    if (*abort_flag) break;
+                    if (!(ok = warp_wait(bar(R_TFREE), (runs - 1) & 1, ws, abort_flag, 4101))) break;
                 }
                 run_seq = r.seq;
                 ++runs;
                 fresh = true;
             }
-            if (lane == 0) lv_wait(bar(R_READY + s), (i / kRStages) & 1, ws, abort_flag, 4102);
-            __syncwarp();
-            if (*abort_flag) break;
+            if (!(ok = warp_wait(bar(R_READY + s), (i / kRStages) & 1, ws, abort_flag, 4102))) break;
             tc::tc_fence_after();
             const uint32_t st = sbase + s * kRStage;
             tc::mma_ss_n<4>(tmem, tc::sdesc(st, 8192, 1024), 128, tc::sdesc(st + 16384, 8192, 1024), 128, kIdKV, !fresh);
             tc::commit_e(bar(R_EMPTY + s));
             fresh = false;
         }
-        if (!*abort_flag && run_seq >= 0) tc::commit_e(bar(R_RUNDONE));
+        if (ok && run_seq >= 0) tc::commit_e(bar(R_RUNDONE));
         tc::commit_e(bar(R_FIN));
         __syncwarp();
     } else if (warp >= 4) {
@@ -170,36 +249,39 @@ kv_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         int run_seq = -1, runs = 0;
         float zsum = 0.f;
         auto flush = [&](int seq) -> bool {
-            if (leader) lv_wait(bar(R_RUNDONE), (runs - 1) & 1, ws, abort_flag, 4103);
-            tc::named_bar(1, 128);
-            if (*abort_flag) return false;
+            if (!group_wait(leader, 1, bar(R_RUNDONE), (runs - 1) & 1, ws, abort_flag, 4103)) return false;
             tc::tc_fence_after();
-            float* dst = kv + (((size_t)seq * H + head) * kD + f) * kD;
+            const size_t slot = GROUPED ? (size_t)blockIdx.x : (size_t)seq;
+            float* dst = kv + ((slot * H + head) * kD + f) * kD;
             float d[32];
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * c, d);
                 tc::tmem_wait_ld();
+                if (GROUPED) {  // this CTA alone owns the group's slot
 #pragma unroll
-                for (int x = 0; x < 32; ++x) atomicAdd(dst + 32 * c + x, d[x]);
+                    for (int x = 0; x < 32; x += 4)
+                        *reinterpret_cast<float4*>(dst + 32 * c + x) = make_float4(d[x], d[x + 1], d[x + 2], d[x + 3]);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) atomicAdd(dst + 32 * c + x, d[x]);
+                }
             }
-            atomicAdd(z + ((size_t)seq * H + head) * kD + f, zsum);
+            if (GROUPED) z[(slot * H + head) * kD + f] = zsum;
+            else atomicAdd(z + (slot * H + head) * kD + f, zsum);
             zsum = 0.f;
             tc::tc_fence_before();
             tc::named_bar(1, 128);
             return true;
         };
-        const uint32_t kcol = (uint32_t)(f >> 6) * 8192 + (uint32_t)((f & 7) * 2);
-        const uint32_t kchunk = (uint32_t)((f & 63) >> 3);
+        bool ok = true;
         for (int i = 0; i < nc; ++i) {
             const int s = i % kRStages;
             const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, g0 + i);
-            if (leader) lv_wait(bar(R_FULL + s), (i / kRStages) & 1, ws, abort_flag, 4104);
-            tc::named_bar(1, 128);
-            if (*abort_flag) break;
+            if (!(ok = group_wait(leader, 1, bar(R_FULL + s), (i / kRStages) & 1, ws, abort_flag, 4104))) break;
             if (r.seq != run_seq) {
                 if (run_seq >= 0) {
-                    if (!flush(run_seq)) break;
+                    if (!(ok = flush(run_seq))) break;
                     if (leader) tc::mbar_arrive(bar(R_TFREE));
                 }
                 run_seq = r.seq;
@@ -212,22 +294,14 @@ kv_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                     tc::st_shared_v4(tc::sw128(st + 16384 + (uint32_t)(c16 >> 3) * 8192, t, c16 & 7), 0u, 0u, 0u, 0u);
                 }
                 tc::fence_proxy_async();
+                tc::named_bar(1, 128);
             }
-            float acc = 0.f;
-            for (int t = 0; t < r.n; ++t) {
-                uint16_t h;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h)
-                             : "r"(st + kcol + (uint32_t)t * 128 + (((kchunk ^ (uint32_t)t) & 7u) << 4)));
-                acc += __bfloat162float(__ushort_as_bfloat16(h));
-            }
-            zsum += acc;
+            if (leader) tc::mbar_arrive(bar(R_READY + s));  // the MMA may take the stage
+            zsum += key_column_sum(st, f, r.n);
             tc::named_bar(1, 128);
-            if (leader) {
-                tc::mbar_arrive(bar(R_READY + s));
-                tc::mbar_arrive(bar(R_EMPTY + s));
-            }
+            if (leader) tc::mbar_arrive(bar(R_EMPTY + s));
         }
-        if (!*abort_flag && run_seq >= 0) flush(run_seq);
+        if (ok && run_seq >= 0) flush(run_seq);
     }
     __syncthreads();
     if (tid == 0) tc::mbar_wait(bar(R_FIN), 0);
@@ -312,16 +386,12 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int s = i % kAStages, b = i & 1;
             const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, g0 + i);
             if (r.seq != run_seq) {  // the workers load this sequence's K^T V first
-                if (lane == 0) lv_wait(bar(A_KVR), runs & 1, ws, abort_flag, 4201);
+                if (!warp_wait(bar(A_KVR), runs & 1, ws, abort_flag, 4201)) break;
                 run_seq = r.seq;
                 ++runs;
             }
-            if (lane == 0) {
-                lv_wait(bar(A_FULL + s), (i / kAStages) & 1, ws, abort_flag, 4202);
-                if (i >= 2) lv_wait(bar(A_EPID + b), ((i >> 1) - 1) & 1, ws, abort_flag, 4203);
-            }
-            __syncwarp();
-            if (*abort_flag) break;
+            if (!warp_wait(bar(A_FULL + s), (i / kAStages) & 1, ws, abort_flag, 4202)) break;
+            if (i >= 2 && !warp_wait(bar(A_EPID + b), ((i >> 1) - 1) & 1, ws, abort_flag, 4203)) break;
             tc::tc_fence_after();
             const uint32_t st = sbase + kAQ + s * 16384, d = tmem + 256u * b;
             tc::mma_ss_n<4>(d, tc::sdesc(st, 16, 1024), 2, tc::sdesc(sbase + kAKVZ, 16384, 1024), 128, kIdQ, false);
@@ -369,9 +439,7 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (leader) tc::mbar_arrive(bar(A_KVR));
                 run_seq = r.seq;
             }
-            if (leader) lv_wait(bar(A_MMAD + b), (i >> 1) & 1, ws, abort_flag, 4204);
-            tc::named_bar(1, 128);
-            if (*abort_flag) break;
+            if (!group_wait(leader, 1, bar(A_MMAD + b), (i >> 1) & 1, ws, abort_flag, 4204)) break;
             tc::tc_fence_after();
             float d[32], e[16];
             uint32_t pk[64];
@@ -422,116 +490,470 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
-// ---------------------------------------------------------------- causal normaliser
-// Sum of the keys of each chunk.
-__global__ void __launch_bounds__(kThreads)
-chunk_key_sum_kernel(const __nv_bfloat16* __restrict__ k, int H, const char* __restrict__ ws,
-                     float* __restrict__ ks) {
-    const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
-    if (hdr->status != GDN_OK || (int)blockIdx.x >= hdr->total_chunks) return;
-    PlanLayout L(hdr->n_seqs);
-    const ChunkRef r = chunk_ref(reinterpret_cast<const int*>(ws + L.cu),
-                                 reinterpret_cast<const int*>(ws + L.chunk_off), hdr->n_seqs, blockIdx.x);
-    const int i = threadIdx.x, head = blockIdx.y;
-    float s = 0.f;
-    for (int t = 0; t < r.n; ++t) s += __bfloat162float(k[((size_t)(r.t0 + t) * H + head) * kD + i]);
-    ks[((size_t)blockIdx.x * H + head) * kD + i] = s;
-}
+// ---------------------------------------------------------------- causal, grouped
+// Causal linear attention without a per-chunk chain across the whole
+// sequence: every sequence is cut into groups of `group` chunks; the groups'
+// K^T V (kv_reduce_kernel<true>) give each group's starting state by a prefix
+// (group_scan_kernel), and every group then runs its own chunks in order from
+// that state (group_apply_kernel), all groups side by side.
 
-// Exclusive prefix of the chunk key sums over each sequence's chunks, and the
-// sequence's total (the summed keys z, when asked for).  One block per
-// (sequence, head, 16 features): each of its 256 threads takes a contiguous
-// run of the sequence's chunks for those 16 features, the runs' totals are
-// scanned in shared memory, and each thread then writes its run's prefixes.
-constexpr int kPrefixThreads = 256, kPrefixFeat = 16;
-__global__ void __launch_bounds__(kPrefixThreads)
-key_prefix_kernel(int H, const char* __restrict__ ws, const float* __restrict__ ks,
-                  float* __restrict__ zstart, float* __restrict__ z) {
-    __shared__ float part[kPrefixThreads][kPrefixFeat + 1];
+// Picks the group size and numbers the groups.  The size is the smallest
+// g >= kMinGroup for which all (sequence, head) pairs together have at most
+// `sms` groups (one wave of one-CTA-per-SM launches), or, when even one group
+// per sequence is more than that, g = max(kMinGroup, ceil(H total / sms)).
+// Either way the group count is at most floor(sms / H) + n_seqs.
+// group_off[s] = first group of sequence s, group_off[n_seqs] = the number of
+// groups, group_off[n_seqs + 1] = the group size.
+__global__ void __launch_bounds__(1024)
+group_plan_kernel(const char* __restrict__ ws, int sms, int H, int* __restrict__ group_off) {
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
-    if (hdr->status != GDN_OK) return;
+    const int n_seqs = hdr->status == GDN_OK ? hdr->n_seqs : 0;
     PlanLayout L(hdr->n_seqs);
     const int* chunk_off = reinterpret_cast<const int*>(ws + L.chunk_off);
-    const int seq = blockIdx.x, head = blockIdx.y, f0 = blockIdx.z * kPrefixFeat, tid = threadIdx.x;
-    const int c0 = chunk_off[seq], nch = chunk_off[seq + 1] - c0;
-    const int per = (nch + kPrefixThreads - 1) / kPrefixThreads;
-    const int a = c0 + min(nch, tid * per), e = c0 + min(nch, (tid + 1) * per);
-    float run[kPrefixFeat];
-#pragma unroll
-    for (int x = 0; x < kPrefixFeat; ++x) run[x] = 0.f;
-    for (int c = a; c < e; ++c) {
-        const float* src = ks + ((size_t)c * H + head) * kD + f0;
-#pragma unroll
-        for (int x = 0; x < kPrefixFeat; ++x) run[x] += src[x];
-    }
-#pragma unroll
-    for (int x = 0; x < kPrefixFeat; ++x) part[tid][x] = run[x];
-    __syncthreads();
-    // inclusive scan of the runs' totals, per feature (Hillis-Steele over 256 entries)
-    for (int off = 1; off < kPrefixThreads; off <<= 1) {
-        float add[kPrefixFeat];
-#pragma unroll
-        for (int x = 0; x < kPrefixFeat; ++x) add[x] = tid >= off ? part[tid - off][x] : 0.f;
+    __shared__ int s_scan[1024];
+    __shared__ int s_carry;
+    __shared__ long long s_red[32];
+    const int tid = threadIdx.x;
+    // number of groups of size g over all sequences (every thread gets it)
+    auto groups_of = [&](long long g) -> long long {
+        long long c = 0;
+        for (int i = tid; i < n_seqs; i += 1024) c += (chunk_off[i + 1] - chunk_off[i] + g - 1) / g;
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
         __syncthreads();
-#pragma unroll
-        for (int x = 0; x < kPrefixFeat; ++x) part[tid][x] += add[x];
+        if ((tid & 31) == 0) s_red[tid >> 5] = c;
         __syncthreads();
-    }
-#pragma unroll
-    for (int x = 0; x < kPrefixFeat; ++x) run[x] = tid > 0 ? part[tid - 1][x] : 0.f;  // before this run
-    for (int c = a; c < e; ++c) {
-        const size_t at = ((size_t)c * H + head) * kD + f0;
-#pragma unroll
-        for (int x = 0; x < kPrefixFeat; ++x) {
-            zstart[at + x] = run[x];
-            run[x] += ks[at + x];
+        long long t = 0;
+        for (int w = 0; w < 32; ++w) t += s_red[w];
+        return t;
+    };
+    const long long total = n_seqs > 0 ? chunk_off[n_seqs] : 0;
+    long long lo = kMinGroup, hi = max((long long)kMinGroup, total);
+    long long group;
+    if ((long long)H * groups_of(hi) <= sms) {
+        while (lo < hi) {  // groups_of is non-increasing in g
+            const long long mid = (lo + hi) >> 1;
+            if ((long long)H * groups_of(mid) <= sms) hi = mid; else lo = mid + 1;
         }
+        group = lo;
+    } else {
+        group = max((long long)kMinGroup, ((long long)H * total + sms - 1) / sms);
     }
-    if (z && tid == kPrefixThreads - 1) {
-#pragma unroll
-        for (int x = 0; x < kPrefixFeat; ++x) z[((size_t)seq * H + head) * kD + f0 + x] = part[tid][x];
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < n_seqs; base += 1024) {
+        const int i = base + tid;
+        const int ng = i < n_seqs ? (int)((chunk_off[i + 1] - chunk_off[i] + group - 1) / group) : 0;
+        s_scan[tid] = ng;
+        __syncthreads();
+        for (int off = 1; off < 1024; off <<= 1) {
+            const int x = tid >= off ? s_scan[tid - off] : 0;
+            __syncthreads();
+            s_scan[tid] += x;
+            __syncthreads();
+        }
+        if (i < n_seqs) group_off[i] = s_carry + s_scan[tid] - ng;
+        __syncthreads();
+        if (tid == 1023) s_carry += s_scan[1023];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        group_off[n_seqs] = s_carry;
+        group_off[n_seqs + 1] = (int)group;
+        if (hdr->status != GDN_OK) group_off[0] = 0;
     }
 }
 
-// o_t /= q_t . (z_start + sum of k_s over s <= t in the chunk), per chunk.
-__global__ void __launch_bounds__(kThreads)
-causal_normalise_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int H,
-                        const char* __restrict__ ws, const float* __restrict__ zstart,
-                        __nv_bfloat16* __restrict__ o) {
-    __shared__ float part[kChunk][kD + 1];
-    const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
-    if (hdr->status != GDN_OK || (int)blockIdx.x >= hdr->total_chunks) return;
-    PlanLayout L(hdr->n_seqs);
-    const ChunkRef r = chunk_ref(reinterpret_cast<const int*>(ws + L.cu),
-                                 reinterpret_cast<const int*>(ws + L.chunk_off), hdr->n_seqs, blockIdx.x);
-    const int i = threadIdx.x, head = blockIdx.y;
-    float zi = zstart[((size_t)blockIdx.x * H + head) * kD + i];
-    for (int t = 0; t < r.n; ++t) {
-        const size_t row = ((size_t)(r.t0 + t) * H + head) * kD;
-        zi += __bfloat162float(k[row + i]);
-        part[t][i] = __bfloat162float(q[row + i]) * zi;
-    }
-    __syncthreads();
-    // two threads per token: features 0..63 and 64..127
-    const int t = i >> 1, half = i & 1;
-    float den = 0.f;
-    if (t < r.n)
-        for (int x = 0; x < 64; ++x) den += part[t][64 * half + x];
-    den += __shfl_xor_sync(0xffffffffu, den, 1);
-    if (t < r.n) {
-        __nv_bfloat16* row = o + ((size_t)(r.t0 + t) * H + head) * kD + 64 * half;
-        const float inv = 1.f / den;
-        for (int x = 0; x < 64; x += 8) {
-            uint4 w = *reinterpret_cast<uint4*>(row + x);
-            uint32_t u[4] = {w.x, w.y, w.z, w.w};
+// Per (sequence, head, 16 state columns): each group's starting state
+// hs[g] = h0 + the K^T V of the sequence's earlier groups (fp32; group g's
+// sum is the two halves Sg[2 g] + Sg[2 g + 1]), the final
+// state h_T, and (slab 0) each group's starting key sum zs[g] and the
+// sequence's total z_T.
+__global__ void __launch_bounds__(kD)
+group_scan_kernel(const char* __restrict__ ws, const int* __restrict__ group_off, int H,
+                  const float* __restrict__ h0, const float* __restrict__ Sg, const float* __restrict__ zg,
+                  float* __restrict__ hs, float* __restrict__ zs, float* __restrict__ h_T,
+                  float* __restrict__ z_T) {
+    if (reinterpret_cast<const WsHeader*>(ws)->status != GDN_OK) return;
+    const int seq = blockIdx.x, head = blockIdx.y, j0 = 16 * blockIdx.z, i = threadIdx.x;
+    float h[16];
 #pragma unroll
-            for (int y = 0; y < 4; ++y) {
-                const float2 f = tc::unpack_bf16(u[y]);
-                u[y] = tc::pack_bf16(f.x * inv, f.y * inv);
-            }
-            *reinterpret_cast<uint4*>(row + x) = make_uint4(u[0], u[1], u[2], u[3]);
+    for (int x = 0; x < 16; ++x)
+        h[x] = h0 ? h0[(((size_t)seq * H + head) * kD + i) * kD + j0 + x] : 0.f;
+    float zacc = 0.f;
+    for (int g = group_off[seq]; g < group_off[seq + 1]; ++g) {
+        const size_t at = (((size_t)g * H + head) * kD + i) * kD + j0;
+        const size_t a0 = (((size_t)(2 * g) * H + head) * kD + i) * kD + j0;
+        const size_t a1 = (((size_t)(2 * g + 1) * H + head) * kD + i) * kD + j0;
+#pragma unroll
+        for (int x = 0; x < 16; x += 4) {
+            *reinterpret_cast<float4*>(hs + at + x) = make_float4(h[x], h[x + 1], h[x + 2], h[x + 3]);
+            const float4 d = *reinterpret_cast<const float4*>(Sg + a0 + x);
+            const float4 e = *reinterpret_cast<const float4*>(Sg + a1 + x);
+            h[x] += d.x + e.x;
+            h[x + 1] += d.y + e.y;
+            h[x + 2] += d.z + e.z;
+            h[x + 3] += d.w + e.w;
+        }
+        if (blockIdx.z == 0) {
+            zs[((size_t)g * H + head) * kD + i] = zacc;
+            zacc += zg[((size_t)(2 * g) * H + head) * kD + i] + zg[((size_t)(2 * g + 1) * H + head) * kD + i];
         }
     }
+    if (h_T) {
+#pragma unroll
+        for (int x = 0; x < 16; x += 4)
+            *reinterpret_cast<float4*>(h_T + (((size_t)seq * H + head) * kD + i) * kD + j0 + x) =
+                make_float4(h[x], h[x + 1], h[x + 2], h[x + 3]);
+    }
+    if (z_T && blockIdx.z == 0) z_T[((size_t)seq * H + head) * kD + i] = zacc;
+}
+
+// Group apply, CTA (g, head), 448 threads: warp 0 TMA, warp 1 MMA, and three
+// 128-thread groups (warps 2..5 the state, 6..9 the P mask, 10..13 the
+// output; warp w reads TMEM lanes 32 (w % 4) ..).  The state S = h^T (lane j
+// = v feature, column i = k feature) accumulates in TMEM in fp32.  Per chunk:
+//   P  = q k^T               (M = 64, N = 64; the P group masks s <= t, s < n
+//                              and stores P in bf16)
+//   S += v^T k               (M = 128, N = 128, fp32)
+//   O  = q [h_c | z_c] + P [v | 1]   (M = 64 over tokens, N = 136, two TMEM buffers)
+// where the state group copies S (the state at the chunk's start) to shared
+// memory in bf16 before the chunk's S update, as a K-major [j][i] tile whose
+// rows 128 and 129 hold the running key sum z_c split into a bf16 high and low
+// part, and every stage carries a fixed column of ones after v.  So O[t][0..127]
+// is the numerator and O[t][128] + O[t][129] the normaliser
+// q_t . z_c + sum_{s <= t} q_t . k_s.  The output group divides (when
+// normalised) and stores o.  Token t of an M = 64 result sits in TMEM lane
+// 32 (t / 16) + t % 16: lanes 0..15 of each warp of the P and output groups.
+constexpr int kGThreads = 448;
+constexpr int kGStages = 2;
+constexpr uint32_t kGStage = 57344;    // q box0 | q box1 | k box0 | k box1 | v box0 | v box1 | ones
+constexpr uint32_t kGSnapBox = 17408;  // 136 rows x 128 B: one 64-column half of [h_c^T ; z_c]
+constexpr uint32_t kGSnap = kGStages * kGStage;  // two snapshots, two halves each
+constexpr uint32_t kGP = kGSnap + 4 * kGSnapBox;  // P, bf16 [t][s]
+constexpr uint32_t kGO = kGP + 8192;              // two o staging tiles, [t][j], two boxes each
+constexpr uint32_t kGBarOff = kGO + 2 * 16384;
+enum {
+    G_FULL = 0, G_EMPTY = 2, G_ZREADY = 4, G_PD = 5, G_PREADY = 6, G_SNAP = 7, G_SD = 8, G_OD = 9, G_OFREE = 11,
+    G_FIN = 13, G_COUNT = 14
+};
+constexpr uint32_t kGSmem = kGBarOff + 128 + 1024;
+static_assert(kGSmem <= 232448, "group apply shared memory");
+static_assert(8 * G_COUNT <= 112, "group apply barriers");
+// TMEM columns: S fp32 0..127 (M = 128), P 128..191 (M = 64), O[0] 192..327, O[1] 352..487 (M = 64)
+constexpr uint32_t kTS32 = 0, kTP = 128, kTO0 = 192, kTO1 = 352;
+constexpr int kGN = 136;
+constexpr uint32_t kGIdP = tc::idesc_bf16(64, 64, false, false);    // A = q, B = k (both K-major)
+constexpr uint32_t kGIdS = tc::idesc_bf16(128, 128, true, true);    // A = v^T, B = k (both MN-major)
+constexpr uint32_t kGIdQ = tc::idesc_bf16(64, kGN, false, false);   // A = q, B = [h_c^T ; z_c] (both K-major)
+constexpr uint32_t kGIdV = tc::idesc_bf16(64, kGN, false, true);    // A = P (K-major), B = [v | 1] (MN-major)
+
+__global__ void __launch_bounds__(kGThreads, 1)
+group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, int H,
+                   char* __restrict__ ws, const int* __restrict__ group_off, const float* __restrict__ hs,
+                   const float* __restrict__ zs, int normalize, __nv_bfloat16* __restrict__ o) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = tc::smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t sbase = raw + pad;
+    char* const sptr = reinterpret_cast<char*>(smem_raw) + pad;
+    const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
+    if (hdr->status != GDN_OK) return;
+    const int n_seqs = hdr->n_seqs, head = blockIdx.y, g = blockIdx.x;
+    if (g >= group_off[n_seqs]) return;
+    PlanLayout L(n_seqs);
+    const int* cu = reinterpret_cast<const int*>(ws + L.cu);
+    const int* chunk_off = reinterpret_cast<const int*>(ws + L.chunk_off);
+    int gseq, c0, nc;
+    group_range(group_off, chunk_off, n_seqs, group_off[n_seqs + 1], g, gseq, c0, nc);
+    if (nc == 0) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    auto bar = [&](int i) { return sbase + kGBarOff + 8u * (uint32_t)i; };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + kGBarOff + 112);
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quadrant
+
+    if (tid == 0) {
+        for (int b = 0; b < G_COUNT; ++b) tc::mbar_init(bar(b), (b == G_EMPTY || b == G_EMPTY + 1) ? 2 : 1);
+        tc::fence_mbar_init();
+        abort_flag[0] = 0;
+        abort_flag[1] = hdr->wait_limit;
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+        tc::prefetch_tmap(&tm_o);
+    }
+    __syncwarp();
+    if (warp == 0) tc::tmem_alloc(sbase + kGBarOff + 120, 512);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t*>(sptr + kGBarOff + 120), 0);
+
+    if (warp == 0) {
+        // ---- TMA: q, k, v of the group's chunks into stage i % kGStages
+        int issued = 0;
+        if (lane == 0) {
+            for (int i = 0; i < nc; ++i) {
+                const int s = i % kGStages;
+                if (i >= kGStages && !lv_wait(bar(G_EMPTY + s), ((i / kGStages) - 1) & 1, ws, abort_flag, 4300)) break;
+                const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
+                const uint32_t st = sbase + s * kGStage;
+                tc::mbar_arrive_expect_tx(bar(G_FULL + s), 49152);
+                tc::tma_load_3d(st, &tm_q, 0, head, r.t0, bar(G_FULL + s));
+                tc::tma_load_3d(st + 8192, &tm_q, 64, head, r.t0, bar(G_FULL + s));
+                tc::tma_load_3d(st + 16384, &tm_k, 0, head, r.t0, bar(G_FULL + s));
+                tc::tma_load_3d(st + 24576, &tm_k, 64, head, r.t0, bar(G_FULL + s));
+                tc::tma_load_3d(st + 32768, &tm_v, 0, head, r.t0, bar(G_FULL + s));
+                tc::tma_load_3d(st + 40960, &tm_v, 64, head, r.t0, bar(G_FULL + s));
+                issued = i + 1;
+            }
+            if (*abort_flag)
+                for (int i = max(0, issued - kGStages); i < issued; ++i)
+                    tc::mbar_wait(bar(G_FULL + i % kGStages), (i / kGStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA, chunk by chunk
+        int npart = 0;
+        for (int i = 0; i < nc; ++i) {
+            const int s = i % kGStages, b = i & 1;
+            const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
+            const uint32_t st = sbase + s * kGStage, q0 = st, k0 = st + 16384, v0 = st + 32768;
+            const uint32_t snap = sbase + kGSnap + 2 * kGSnapBox * (uint32_t)b;
+            const uint32_t dO = tmem + (b ? kTO1 : kTO0);
+            if (!warp_wait(bar(G_FULL + s), (i / kGStages) & 1, ws, abort_flag, 4301)) break;
+            if (r.n < kChunk) {  // the state group first zeroes the rows past the sequence's end
+                if (!warp_wait(bar(G_ZREADY), npart & 1, ws, abort_flag, 4302)) break;
+                ++npart;
+            }
+            tc::tc_fence_after();
+            // P = q k^T
+            tc::mma_ss_n<4>(tmem + kTP, tc::sdesc(q0, 16, 1024), 2, tc::sdesc(k0, 16, 1024), 2, kGIdP, false);
+            tc::mma_ss_n<4>(tmem + kTP, tc::sdesc(q0 + 8192, 16, 1024), 2, tc::sdesc(k0 + 8192, 16, 1024), 2, kGIdP,
+                            true);
+            tc::commit_e(bar(G_PD));
+            // S += v^T k once the state at this chunk's start has been copied out
+            if (!warp_wait(bar(G_SNAP), i & 1, ws, abort_flag, 4303)) break;
+            tc::tc_fence_after();
+            tc::mma_ss_n<4>(tmem + kTS32, tc::sdesc(v0, 8192, 1024), 128, tc::sdesc(k0, 8192, 1024), 128, kGIdS, true);
+            tc::commit_e(bar(G_SD));
+            // O[b] = q [h_c | z_c] once chunk i - 2's O[b] has been read
+            if (i >= 2 && !warp_wait(bar(G_OFREE + b), ((i >> 1) - 1) & 1, ws, abort_flag, 4304)) break;
+            tc::tc_fence_after();
+            tc::mma_ss_n<4>(dO, tc::sdesc(q0, 16, 1024), 2, tc::sdesc(snap, 16, 1024), 2, kGIdQ, false);
+            tc::mma_ss_n<4>(dO, tc::sdesc(q0 + 8192, 16, 1024), 2, tc::sdesc(snap + kGSnapBox, 16, 1024), 2, kGIdQ,
+                            true);
+            // O[b] += P [v | 1] once P is masked and stored
+            if (!warp_wait(bar(G_PREADY), i & 1, ws, abort_flag, 4305)) break;
+            tc::tc_fence_after();
+            tc::mma_ss_n<4>(dO, tc::sdesc(sbase + kGP, 16, 1024), 2, tc::sdesc(v0, 8192, 1024), 128, kGIdV, true);
+            tc::commit_e(bar(G_OD + b));
+            tc::commit_e(bar(G_EMPTY + s));
+        }
+        tc::commit_e(bar(G_FIN));
+        __syncwarp();
+    } else if (warp < 6) {
+        // ---- state group: thread f owns state row j = f (a TMEM lane) and key-sum entry z[f]
+        const int f = 32 * (warp & 3) + lane;
+        const bool leader = warp == 2 && lane == 0;
+        // row f of a snapshot half from 64 fp32 values (columns 64 half .. 64 half + 63)
+        auto snap_half = [&](uint32_t snap, int half, const float (&x)[64]) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                tc::st_shared_v4(tc::sw128(snap + (uint32_t)half * kGSnapBox, f, c), tc::pack_bf16(x[8 * c], x[8 * c + 1]),
+                                 tc::pack_bf16(x[8 * c + 2], x[8 * c + 3]), tc::pack_bf16(x[8 * c + 4], x[8 * c + 5]),
+                                 tc::pack_bf16(x[8 * c + 6], x[8 * c + 7]));
+        };
+        // entry f of the key sum, high and low bf16 parts, into rows 128 and 129
+        auto snap_z = [&](uint32_t snap, float zf) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(zf);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(zf - __bfloat162float(hi));
+            const uint32_t box = snap + (uint32_t)(f >> 6) * kGSnapBox, c = (uint32_t)((f & 63) >> 3);
+            const uint32_t e = (uint32_t)(f & 7) * 2;
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(tc::sw128(box, 128, c) + e), "h"(__bfloat16_as_ushort(hi)) : "memory");
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(tc::sw128(box, 129, c) + e), "h"(__bfloat16_as_ushort(lo)) : "memory");
+        };
+        // fixed parts: the ones column after v in both stages (row s, column 0 of the
+        // third box), rows 128..135 of both snapshots zero
+        for (int x = f; x < kGStages * 64 * 8; x += 128) {
+            const int stg = x >> 9, row = (x >> 3) & 63, c = x & 7;
+            tc::st_shared_v4(sbase + (uint32_t)stg * kGStage + 49152 + (uint32_t)row * 128 + (uint32_t)c * 16,
+                             c == (row & 7) ? 0x3F80u : 0u, 0u, 0u, 0u);
+        }
+        for (int x = f; x < 4 * 8 * 8; x += 128) {
+            const int box = x >> 6, row = 128 + ((x >> 3) & 7), c = x & 7;
+            tc::st_shared_v4(sbase + kGSnap + (uint32_t)box * kGSnapBox + (uint32_t)row * 128 + (uint32_t)c * 16, 0u,
+                             0u, 0u, 0u);
+        }
+        float zf = 0.f;
+        {  // S and the first snapshot from the group's starting state (h[i][j] -> S[j][i])
+            const float* hsrc = hs + ((size_t)g * H + head) * kD * kD;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                float x[64];
+#pragma unroll
+                for (int i2 = 0; i2 < 64; ++i2) x[i2] = hsrc[(size_t)(64 * half + i2) * kD + f];
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) r[e2] = __float_as_uint(x[16 * part + e2]);
+                    tc::tmem_st16(tmem + lane_off + kTS32 + 64 * half + 16 * part, r);
+                }
+                snap_half(sbase + kGSnap, half, x);
+            }
+            tc::tmem_wait_st();
+            tc::named_bar(1, 128);  // rows 128..135 were zeroed by other threads: the z rows come after
+            if (normalize) {
+                zf = zs[((size_t)g * H + head) * kD + f];
+                snap_z(sbase + kGSnap, zf);
+            }
+            tc::fence_proxy_async();
+            tc::tc_fence_before();
+            tc::named_bar(1, 128);
+            if (leader) tc::mbar_arrive(bar(G_SNAP));
+        }
+        for (int i = 0; i < nc; ++i) {
+            const int s = i % kGStages;
+            const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
+            const uint32_t st = sbase + s * kGStage, k0 = st + 16384;
+            if (!group_wait(leader, 1, bar(G_FULL + s), (i / kGStages) & 1, ws, abort_flag, 4306)) break;
+            if (r.n < kChunk) {  // rows past a partial chunk's end belong to the next sequence: zero them in k and v
+                for (int x = f; x < (kChunk - r.n) * 32; x += 128) {
+                    const int t = r.n + (x >> 5), c32 = x & 31;  // 16-byte chunk c32 of k (0..15) or v (16..31)
+                    const uint32_t base = (c32 < 16 ? k0 : st + 32768) + (uint32_t)((c32 & 15) >> 3) * 8192;
+                    tc::st_shared_v4(tc::sw128(base, t, c32 & 7), 0u, 0u, 0u, 0u);
+                }
+                tc::fence_proxy_async();
+                tc::named_bar(1, 128);
+                if (leader) tc::mbar_arrive(bar(G_ZREADY));
+            }
+            const float zc = normalize ? key_column_sum(k0, f, r.n) : 0.f;
+            if (i + 1 < nc) {
+                // the state after this chunk, for the next one
+                if (!group_wait(leader, 1, bar(G_SD), i & 1, ws, abort_flag, 4307)) break;
+                tc::tc_fence_after();
+                const uint32_t snap = sbase + kGSnap + 2 * kGSnapBox * (uint32_t)((i + 1) & 1);
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    float x[64], y[32];
+                    tc::tmem_ld32(tmem + lane_off + kTS32 + 64 * half, y);
+                    tc::tmem_ld32(tmem + lane_off + kTS32 + 64 * half + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int e2 = 0; e2 < 32; ++e2) x[e2] = y[e2];
+                    snap_half(snap, half, x);
+                }
+                if (normalize) {
+                    zf += zc;
+                    snap_z(snap, zf);
+                }
+                tc::fence_proxy_async();
+                tc::tc_fence_before();
+                tc::named_bar(1, 128);
+                if (leader) {
+                    tc::mbar_arrive(bar(G_SNAP));
+                    tc::mbar_arrive(bar(G_EMPTY + s));
+                }
+            } else {
+                tc::named_bar(1, 128);
+                if (leader) tc::mbar_arrive(bar(G_EMPTY + s));
+            }
+        }
+    } else if (warp < 10) {
+        // ---- P group: mask s <= t, s < n; bf16 tile for the P [v | 1] MMA
+        const bool leader = warp == 6 && lane == 0;
+        const int tP = 16 * (warp & 3) + lane;  // this lane's token (lanes < 16)
+        for (int i = 0; i < nc; ++i) {
+            const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
+            if (!group_wait(leader, 2, bar(G_PD), i & 1, ws, abort_flag, 4308)) break;
+            tc::tc_fence_after();
+            float p[32], p2[32];
+            tc::tmem_ld32(tmem + lane_off + kTP, p);
+            tc::tmem_ld32(tmem + lane_off + kTP + 32, p2);
+            tc::tmem_wait_ld();
+            if (lane < 16) {
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float w[8];
+#pragma unroll
+                    for (int e2 = 0; e2 < 8; ++e2) {
+                        const int sc = 8 * c8 + e2;
+                        const float pv = c8 < 4 ? p[sc] : p2[sc - 32];
+                        w[e2] = (sc <= tP && sc < r.n) ? pv : 0.f;
+                    }
+                    tc::st_shared_v4(tc::sw128(sbase + kGP, tP, c8), tc::pack_bf16(w[0], w[1]), tc::pack_bf16(w[2], w[3]),
+                                     tc::pack_bf16(w[4], w[5]), tc::pack_bf16(w[6], w[7]));
+                }
+            }
+            tc::fence_proxy_async();
+            tc::tc_fence_before();
+            tc::named_bar(2, 128);
+            if (leader) tc::mbar_arrive(bar(G_PREADY));
+        }
+    } else {
+        // ---- output group: o = O / den, staged and stored with TMA (a partial chunk directly)
+        const bool leader = warp == 10 && lane == 0;
+        const int tP = 16 * (warp & 3) + lane;
+        for (int i = 0; i < nc; ++i) {
+            const int b = i & 1;
+            const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
+            const uint32_t tO = tmem + lane_off + (b ? kTO1 : kTO0), stage_o = sbase + kGO + 16384u * (uint32_t)b;
+            if (leader) tc::bulk_wait_read1();  // the store from this staging tile two chunks back is done reading it
+            if (!group_wait(leader, 3, bar(G_OD + b), (i >> 1) & 1, ws, abort_flag, 4309)) break;
+            tc::tc_fence_after();
+            float inv = 1.f;
+            if (normalize) {
+                float dz[16];
+                tc::tmem_ld16(tO + 128, dz);
+                tc::tmem_wait_ld();
+                inv = 1.f / (dz[0] + dz[1]);
+            }
+            const bool full = r.n == kChunk;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                float y[32], y2[32];
+                tc::tmem_ld32(tO + 64 * half, y);
+                tc::tmem_ld32(tO + 64 * half + 32, y2);
+                tc::tmem_wait_ld();
+                uint32_t pk[32];
+#pragma unroll
+                for (int e2 = 0; e2 < 16; ++e2) {
+                    pk[e2] = tc::pack_bf16(y[2 * e2] * inv, y[2 * e2 + 1] * inv);
+                    pk[16 + e2] = tc::pack_bf16(y2[2 * e2] * inv, y2[2 * e2 + 1] * inv);
+                }
+                if (full) {
+                    if (lane < 16) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            tc::st_shared_v4(tc::sw128(stage_o + (uint32_t)half * 8192, tP, c), pk[4 * c], pk[4 * c + 1],
+                                             pk[4 * c + 2], pk[4 * c + 3]);
+                    }
+                } else if (lane < 16 && tP < r.n) {  // the last, partial chunk of a sequence
+                    uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(r.t0 + tP) * H + head) * kD + 64 * half);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
+            }
+            tc::fence_proxy_async();
+            tc::tc_fence_before();
+            tc::named_bar(3, 128);
+            if (leader) {
+                tc::mbar_arrive(bar(G_OFREE + b));
+                if (full) {
+                    tc::tma_store_3d(&tm_o, stage_o, 0, head, r.t0);
+                    tc::tma_store_3d(&tm_o, stage_o + 8192, 64, head, r.t0);
+                    tc::bulk_commit();
+                }
+            }
+        }
+        if (leader) tc::bulk_wait0();
+    }
+    __syncthreads();
+    if (tid == 0) tc::mbar_wait(bar(G_FIN), 0);
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 }  // namespace linvar
@@ -541,7 +963,8 @@ bool linear_variant_shape_ok(const PrefillArgs& a) { return a.io == GDN_BF16 && 
 
 size_t linear_variant_extra_bytes(int64_t T, int H, int n_seqs, bool causal) {
     const size_t nch = (size_t)max_chunks(T, n_seqs);
-    if (causal) return 2 * align256(sizeof(float) * nch * H * linvar::kD);  // chunk key sums, prefixes
+    (void)nch;
+    if (causal) return linear_grouped_extra_bytes(T, H, n_seqs);
     return align256(sizeof(float) * (size_t)n_seqs * H * linvar::kD * linvar::kD) +
            align256(sizeof(float) * (size_t)n_seqs * H * linvar::kD);  // K^T V, summed keys
 }
@@ -566,9 +989,10 @@ cudaError_t launch_linear_bidirectional(const PrefillArgs& a, char* plan_ws, cha
         if (!encode_token_map(&mq, a.q, a.T_total, a.H) || !encode_token_map(&mk, a.k, a.T_total, a.H) ||
             !encode_token_map(&mv, a.v, a.T_total, a.H) || !encode_token_map(&mo, a.o, a.T_total, a.H))
             return cudaErrorInvalidValue;
-        e = cudaFuncSetAttribute(kv_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmem);
+        e = cudaFuncSetAttribute(kv_reduce_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmem);
         if (e == cudaSuccess) {
-            kv_reduce_kernel<<<dim3(groups, a.H), kLvThreads, kRSmem, st>>>(mk, mv, a.H, group, plan_ws, kv, z);
+            kv_reduce_kernel<false><<<dim3(groups, a.H), kLvThreads, kRSmem, st>>>(mk, mv, a.H, group, plan_ws,
+                                                                                   nullptr, kv, z);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess)
@@ -584,26 +1008,64 @@ cudaError_t launch_linear_bidirectional(const PrefillArgs& a, char* plan_ws, cha
     return e;
 }
 
-cudaError_t launch_linear_causal_normaliser(const PrefillArgs& a, char* plan_ws, char* extra, bool divide,
-                                            float* z_out, cudaStream_t st) {
+// Groups of the causal path: group_plan_kernel picks the size on the device,
+// with at most floor(sms / H) + n_seqs groups in all.
+static long long max_groups(int H, int n_seqs) {
+    const long long sms = sm_count() > 0 ? sm_count() : 148;
+    return sms / (H > 0 ? H : 1) + n_seqs;
+}
+
+size_t linear_grouped_extra_bytes(int64_t T, int H, int n_seqs) {
+    (void)T;
+    const size_t ng = (size_t)max_groups(H, n_seqs);
+    // group_off, the half-group sums Sg (2 per group), the starting states hs,
+    // the half-group key sums zg (2 per group), the starting key sums zs
+    return align256(sizeof(int) * (size_t)(n_seqs + 2)) + align256(sizeof(float) * 2 * ng * H * linvar::kD * linvar::kD) +
+           align256(sizeof(float) * ng * H * linvar::kD * linvar::kD) + align256(sizeof(float) * 2 * ng * H * linvar::kD) +
+           align256(sizeof(float) * ng * H * linvar::kD);
+}
+
+cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* extra, bool normalize, float* h_T,
+                                  float* z_T, cudaStream_t st) {
     using namespace linvar;
-    const size_t nch = (size_t)max_chunks(a.T_total, a.n_seqs);
-    if (nch == 0) return cudaSuccess;
-    float* ks = reinterpret_cast<float*>(extra);
-    float* zstart = reinterpret_cast<float*>(extra + align256(sizeof(float) * nch * a.H * kD));
-    chunk_key_sum_kernel<<<dim3((unsigned)nch, a.H), kThreads, 0, st>>>((const __nv_bfloat16*)a.k, a.H, plan_ws, ks);
+    const size_t ng = (size_t)max_groups(a.H, a.n_seqs);
+    const int sms = sm_count() > 0 ? sm_count() : 148;
+    int* group_off = reinterpret_cast<int*>(extra);
+    char* p = extra + align256(sizeof(int) * (size_t)(a.n_seqs + 2));
+    float* Sg = reinterpret_cast<float*>(p);
+    p += align256(sizeof(float) * 2 * ng * a.H * kD * kD);
+    float* hs = reinterpret_cast<float*>(p);
+    p += align256(sizeof(float) * ng * a.H * kD * kD);
+    float* zg = reinterpret_cast<float*>(p);
+    p += align256(sizeof(float) * 2 * ng * a.H * kD);
+    float* zs = reinterpret_cast<float*>(p);
+    if (a.n_seqs == 0) return cudaSuccess;
+    group_plan_kernel<<<1, 1024, 0, st>>>(plan_ws, sms, a.H, group_off);
     cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess && a.n_seqs > 0) {
-        key_prefix_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / kPrefixFeat), kPrefixThreads, 0, st>>>(
-            a.H, plan_ws, ks, zstart, z_out);
-        e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (a.T_total > 0) {
+        CUtensorMap mq, mk, mv, mo;
+        if (!encode_token_map(&mq, a.q, a.T_total, a.H) || !encode_token_map(&mk, a.k, a.T_total, a.H) ||
+            !encode_token_map(&mv, a.v, a.T_total, a.H) || !encode_token_map(&mo, a.o, a.T_total, a.H))
+            return cudaErrorInvalidValue;
+        e = cudaFuncSetAttribute(kv_reduce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmem);
+        if (e != cudaSuccess) return e;
+        kv_reduce_kernel<true><<<dim3((unsigned)(2 * ng), a.H), kLvThreads, kRSmem, st>>>(mk, mv, a.H, 0, plan_ws,
+                                                                                   group_off, Sg, zg);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / 16), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0, Sg,
+                                                                                 zg, hs, zs, h_T, z_T);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(group_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+        if (e != cudaSuccess) return e;
+        group_apply_kernel<<<dim3((unsigned)ng, a.H), kGThreads, kGSmem, st>>>(
+            mq, mk, mv, mo, a.H, plan_ws, group_off, hs, zs, normalize ? 1 : 0, (__nv_bfloat16*)a.o);
+        return cudaGetLastError();
     }
-    if (e == cudaSuccess && divide) {
-        causal_normalise_kernel<<<dim3((unsigned)nch, a.H), kThreads, 0, st>>>(
-            (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, a.H, plan_ws, zstart, (__nv_bfloat16*)a.o);
-        e = cudaGetLastError();
-    }
-    return e;
+    // no tokens: every final state is its initial state, every key sum zero
+    group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / 16), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0, Sg, zg,
+                                                                             hs, zs, h_T, z_T);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn

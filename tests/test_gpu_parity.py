@@ -116,6 +116,7 @@ KERNELS = [pytest.param(("1", "1"), id="pair_1solve"), pytest.param(("1", "2"), 
 
 
 def use_kernel(monkeypatch, kernel):
+    monkeypatch.setenv("GDN_LINEAR_PATH", "cluster")  # linear attention through the fused kernels too
     monkeypatch.setenv("GDN_PREFILL_PAIR", kernel[0])
     if kernel[1] is None:
         monkeypatch.delenv("GDN_PREFILL_FRONTS", raising=False)
@@ -460,6 +461,77 @@ def test_linear_bidirectional_forced_timeout_then_recovery(g):
     ro, _, _ = oracle.linear_variant(inp["q"], inp["k"], inp["v"], inp["cu_seqlens"], causal=False,
                                      normalize=True)
     assert rel(o, ro) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ causal linear attention, grouped
+
+@pytest.mark.parametrize("lengths,H,h0_std", [([1, 100, 0, 257, 64, 700], 4, 0.5), ([3000, 1500], 8, 0.0),
+                                              ([64, 65, 63, 128, 1], 4, 0.1)])
+def test_linear_grouped_against_oracle(g, monkeypatch, lengths, H, h0_std):
+    """Causal linear attention through groups of chunks (the default path of
+    linear_attn_fwd for bf16, d = 128): ragged sequences, several groups per
+    sequence, partial and empty chunks, with and without h0; every output and
+    every final state against the oracle's recurrence."""
+    monkeypatch.delenv("GDN_LINEAR_PATH", raising=False)
+    monkeypatch.delenv("GDN_PREFILL_PAIR", raising=False)
+    monkeypatch.delenv("GDN_TWO_LEVEL", raising=False)
+    inp = gi.linear_inputs(lengths, H, 128, 128, "bf16", h0_std=h0_std, seed=61)
+    d = dev(inp)
+    o, hT, ws = g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"])
+    assert g.workspace_status(ws) == 0
+    ro, rh = oracle.linear(inp["q"], inp["k"], inp["v"], inp["h0"], inp["cu_seqlens"])
+    assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
+    assert rel(hT, rh) <= TOL["bf16"], rel(hT, rh)
+
+
+def test_linear_grouped_many_sequences(g, monkeypatch):
+    """More (sequence, head) pairs than SMs (44 sequences x 4 heads), so the
+    group size comes from the total, not from the one-wave search: every
+    output and final state, normalised and not, against the oracle."""
+    monkeypatch.delenv("GDN_LINEAR_PATH", raising=False)
+    lengths = [int(x) for x in torch.randint(1, 700, (44,), generator=torch.Generator().manual_seed(64))]
+    inp = gi.linear_inputs(lengths, 4, 128, 128, "bf16", h0_std=0.1, seed=64)
+    d = dev(inp)
+    o, hT, ws = g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"])
+    assert g.workspace_status(ws) == 0
+    ro, rh = oracle.linear(inp["q"], inp["k"], inp["v"], inp["h0"], inp["cu_seqlens"])
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
+    on, _, _, ws = g.linear_attn_variant(d["q"], d["k"], d["v"], d["cu_seqlens"], causal=True, normalize=True)
+    assert g.workspace_status(ws) == 0
+    rn, _, _ = oracle.linear_variant(inp["q"], inp["k"], inp["v"], inp["cu_seqlens"], causal=True, normalize=True)
+    assert rel(on, rn) <= TOL["bf16"], rel(on, rn)
+
+
+def test_linear_grouped_t131072_h32(g, monkeypatch):
+    """One 131072-token sequence, H = 32, through groups: sampled heads, every
+    token, and all final states against the oracle."""
+    monkeypatch.delenv("GDN_LINEAR_PATH", raising=False)
+    inp = gi.linear_inputs([131072], 32, 128, 128, "bf16", h0_std=0.1, seed=62)
+    d = dev(inp)
+    o, hT, ws = g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"])
+    assert g.workspace_status(ws) == 0
+    hs = [0, 19]
+    ro, rh = oracle.linear(inp["q"][:, hs], inp["k"][:, hs], inp["v"][:, hs], inp["h0"][:, hs])
+    assert rel(o[:, hs], ro) <= TOL["bf16"] and rel(hT[:, hs], rh) <= TOL["bf16"]
+    rkv, _ = oracle.linear_sums(inp["k"], inp["v"])
+    assert rel(hT, inp["h0"].double().numpy() + rkv) <= TOL["bf16"]
+
+
+def test_linear_grouped_forced_timeout_then_recovery(g, monkeypatch):
+    monkeypatch.delenv("GDN_LINEAR_PATH", raising=False)
+    inp = gi.linear_inputs([700, 300], 4, 128, 128, "bf16", h0_std=0.1, seed=63)
+    d = dev(inp)
+    args = [d[k] for k in ("q", "k", "v", "h0", "cu_seqlens")]
+    old = g.set_wait_limit(0)
+    try:
+        _, _, ws = g.linear_attn_fwd(*args)
+        assert g.workspace_status(ws) in (0, -9)
+    finally:
+        g.set_wait_limit(old)
+    o, hT, _ = g.linear_attn_fwd(*args, workspace=ws)
+    assert g.workspace_status(ws) == 0
+    ro, rh = oracle.linear(inp["q"], inp["k"], inp["v"], inp["h0"], inp["cu_seqlens"])
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
 
 
 # ------------------------------------------------------------------ failure detection
