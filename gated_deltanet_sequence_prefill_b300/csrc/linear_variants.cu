@@ -512,37 +512,50 @@ group_plan_kernel(const char* __restrict__ ws, int sms, int H, int* __restrict__
     const int* chunk_off = reinterpret_cast<const int*>(ws + L.chunk_off);
     __shared__ int s_scan[1024];
     __shared__ int s_carry;
-    __shared__ long long s_red[32];
+    __shared__ int s_red[2][32];
     const int tid = threadIdx.x;
-    // number of groups of size g over all sequences (every thread gets it)
-    auto groups_of = [&](long long g) -> long long {
-        long long c = 0;
-        for (int i = tid; i < n_seqs; i += 1024) c += (chunk_off[i + 1] - chunk_off[i] + g - 1) / g;
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        __syncthreads();
-        if ((tid & 31) == 0) s_red[tid >> 5] = c;
-        __syncthreads();
-        long long t = 0;
-        for (int w = 0; w < 32; ++w) t += s_red[w];
+    // this thread's sequences' chunk counts (the first 8 x 1024 kept in registers)
+    constexpr int kKeep = 8;
+    int cnt[kKeep];
+#pragma unroll
+    for (int k = 0; k < kKeep; ++k) {
+        const int i = tid + 1024 * k;
+        cnt[k] = i < n_seqs ? chunk_off[i + 1] - chunk_off[i] : 0;
+    }
+    // number of groups of size g over all sequences (every thread gets it; the
+    // count is at most the number of chunks, which fits an int)
+    int flip = 0;
+    auto groups_of = [&](int g) -> int {
+        int c = 0;
+#pragma unroll
+        for (int k = 0; k < kKeep; ++k) c += (cnt[k] + g - 1) / g;
+        for (int i = tid + 1024 * kKeep; i < n_seqs; i += 1024) c += (chunk_off[i + 1] - chunk_off[i] + g - 1) / g;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if ((tid & 31) == 0) s_red[flip][tid >> 5] = c;
+        __syncthreads();  // alternate buffers: one barrier per evaluation
+        int t = 0;
+#pragma unroll
+        for (int w = 0; w < 32; ++w) t += s_red[flip][w];
+        flip ^= 1;
         return t;
     };
-    const long long total = n_seqs > 0 ? chunk_off[n_seqs] : 0;
-    long long lo = kMinGroup, hi = max((long long)kMinGroup, total);
-    long long group;
+    const int total = n_seqs > 0 ? chunk_off[n_seqs] : 0;
+    int lo = kMinGroup, hi = max(kMinGroup, total);
+    int group;
     if ((long long)H * groups_of(hi) <= sms) {
         while (lo < hi) {  // groups_of is non-increasing in g
-            const long long mid = (lo + hi) >> 1;
+            const int mid = (lo + hi) >> 1;
             if ((long long)H * groups_of(mid) <= sms) hi = mid; else lo = mid + 1;
         }
         group = lo;
     } else {
-        group = max((long long)kMinGroup, ((long long)H * total + sms - 1) / sms);
+        group = (int)max((long long)kMinGroup, ((long long)H * total + sms - 1) / sms);
     }
     if (tid == 0) s_carry = 0;
     __syncthreads();
     for (int base = 0; base < n_seqs; base += 1024) {
         const int i = base + tid;
-        const int ng = i < n_seqs ? (int)((chunk_off[i + 1] - chunk_off[i] + group - 1) / group) : 0;
+        const int ng = i < n_seqs ? (chunk_off[i + 1] - chunk_off[i] + group - 1) / group : 0;
         s_scan[tid] = ng;
         __syncthreads();
         for (int off = 1; off < 1024; off <<= 1) {
@@ -558,54 +571,75 @@ group_plan_kernel(const char* __restrict__ ws, int sms, int H, int* __restrict__
     }
     if (tid == 0) {
         group_off[n_seqs] = s_carry;
-        group_off[n_seqs + 1] = (int)group;
+        group_off[n_seqs + 1] = group;
         if (hdr->status != GDN_OK) group_off[0] = 0;
     }
 }
 
-// Per (sequence, head, 16 state columns): each group's starting state
+// Per (sequence, head, 8 state columns): each group's starting state
 // hs[g] = h0 + the K^T V of the sequence's earlier groups (fp32; group g's
-// sum is the two halves Sg[2 g] + Sg[2 g + 1]), the final
-// state h_T, and (slab 0) each group's starting key sum zs[g] and the
-// sequence's total z_T.
+// sum is the two halves Sg[2 g] + Sg[2 g + 1]), the final state h_T, and
+// (slab 0) each group's starting key sum zs[g] and the sequence's total z_T.
+// The groups go four at a time, every load of the four issued before the
+// running sum takes them.
+constexpr int kScanCols = 8, kScanBatch = 4;
 __global__ void __launch_bounds__(kD)
 group_scan_kernel(const char* __restrict__ ws, const int* __restrict__ group_off, int H,
                   const float* __restrict__ h0, const float* __restrict__ Sg, const float* __restrict__ zg,
                   float* __restrict__ hs, float* __restrict__ zs, float* __restrict__ h_T,
                   float* __restrict__ z_T) {
     if (reinterpret_cast<const WsHeader*>(ws)->status != GDN_OK) return;
-    const int seq = blockIdx.x, head = blockIdx.y, j0 = 16 * blockIdx.z, i = threadIdx.x;
-    float h[16];
+    const int seq = blockIdx.x, head = blockIdx.y, j0 = kScanCols * blockIdx.z, i = threadIdx.x;
+    const bool zslab = blockIdx.z == 0;
+    auto row = [&](int slot) { return (((size_t)slot * H + head) * kD + i) * kD + j0; };
+    float h[kScanCols];
 #pragma unroll
-    for (int x = 0; x < 16; ++x)
-        h[x] = h0 ? h0[(((size_t)seq * H + head) * kD + i) * kD + j0 + x] : 0.f;
+    for (int x = 0; x < kScanCols; ++x) h[x] = h0 ? h0[row(seq) + x] : 0.f;
     float zacc = 0.f;
-    for (int g = group_off[seq]; g < group_off[seq + 1]; ++g) {
-        const size_t at = (((size_t)g * H + head) * kD + i) * kD + j0;
-        const size_t a0 = (((size_t)(2 * g) * H + head) * kD + i) * kD + j0;
-        const size_t a1 = (((size_t)(2 * g + 1) * H + head) * kD + i) * kD + j0;
+    const int gb = group_off[seq], ge = group_off[seq + 1];
+    for (int g = gb; g < ge; g += kScanBatch) {
+        float d[kScanBatch][kScanCols], dz[kScanBatch];
 #pragma unroll
-        for (int x = 0; x < 16; x += 4) {
-            *reinterpret_cast<float4*>(hs + at + x) = make_float4(h[x], h[x + 1], h[x + 2], h[x + 3]);
-            const float4 d = *reinterpret_cast<const float4*>(Sg + a0 + x);
-            const float4 e = *reinterpret_cast<const float4*>(Sg + a1 + x);
-            h[x] += d.x + e.x;
-            h[x + 1] += d.y + e.y;
-            h[x + 2] += d.z + e.z;
-            h[x + 3] += d.w + e.w;
+        for (int u = 0; u < kScanBatch; ++u) {
+            const bool on = g + u < ge;
+#pragma unroll
+            for (int x = 0; x < kScanCols; x += 4) {
+                float4 p = make_float4(0.f, 0.f, 0.f, 0.f), q = p;
+                if (on) {
+                    p = *reinterpret_cast<const float4*>(Sg + row(2 * (g + u)) + x);
+                    q = *reinterpret_cast<const float4*>(Sg + row(2 * (g + u) + 1) + x);
+                }
+                d[u][x] = p.x + q.x;
+                d[u][x + 1] = p.y + q.y;
+                d[u][x + 2] = p.z + q.z;
+                d[u][x + 3] = p.w + q.w;
+            }
+            dz[u] = (on && zslab) ? zg[((size_t)(2 * (g + u)) * H + head) * kD + i] +
+                                        zg[((size_t)(2 * (g + u) + 1) * H + head) * kD + i]
+                                  : 0.f;
         }
-        if (blockIdx.z == 0) {
-            zs[((size_t)g * H + head) * kD + i] = zacc;
-            zacc += zg[((size_t)(2 * g) * H + head) * kD + i] + zg[((size_t)(2 * g + 1) * H + head) * kD + i];
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) {
+            if (g + u >= ge) break;
+            float* dst = hs + row(g + u);
+#pragma unroll
+            for (int x = 0; x < kScanCols; x += 4) {
+                *reinterpret_cast<float4*>(dst + x) = make_float4(h[x], h[x + 1], h[x + 2], h[x + 3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) h[x + e] += d[u][x + e];
+            }
+            if (zslab) {
+                zs[((size_t)(g + u) * H + head) * kD + i] = zacc;
+                zacc += dz[u];
+            }
         }
     }
     if (h_T) {
 #pragma unroll
-        for (int x = 0; x < 16; x += 4)
-            *reinterpret_cast<float4*>(h_T + (((size_t)seq * H + head) * kD + i) * kD + j0 + x) =
-                make_float4(h[x], h[x + 1], h[x + 2], h[x + 3]);
+        for (int x = 0; x < kScanCols; x += 4)
+            *reinterpret_cast<float4*>(h_T + row(seq) + x) = make_float4(h[x], h[x + 1], h[x + 2], h[x + 3]);
     }
-    if (z_T && blockIdx.z == 0) z_T[((size_t)seq * H + head) * kD + i] = zacc;
+    if (z_T && zslab) z_T[((size_t)seq * H + head) * kD + i] = zacc;
 }
 
 // Group apply, CTA (g, head), 448 threads: warp 0 TMA, warp 1 MMA, and three
@@ -1053,7 +1087,7 @@ cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* ext
         kv_reduce_kernel<true><<<dim3((unsigned)(2 * ng), a.H), kLvThreads, kRSmem, st>>>(mk, mv, a.H, 0, plan_ws,
                                                                                    group_off, Sg, zg);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / 16), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0, Sg,
+        group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / kScanCols), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0, Sg,
                                                                                  zg, hs, zs, h_T, z_T);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         e = cudaFuncSetAttribute(group_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
@@ -1063,7 +1097,7 @@ cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* ext
         return cudaGetLastError();
     }
     // no tokens: every final state is its initial state, every key sum zero
-    group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / 16), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0, Sg, zg,
+    group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / kScanCols), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0, Sg, zg,
                                                                              hs, zs, h_T, z_T);
     return cudaGetLastError();
 }
