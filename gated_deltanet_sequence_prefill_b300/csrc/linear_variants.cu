@@ -20,6 +20,8 @@
 // by side (the causal normaliser q_t . (sum of k_s, s <= t) comes out of the
 // same pass).
 #include <cuda_runtime.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <cuda.h>
 
@@ -264,7 +266,10 @@ kv_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                         *reinterpret_cast<float4*>(dst + 32 * c + x) = make_float4(d[x], d[x + 1], d[x + 2], d[x + 3]);
                 } else {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) atomicAdd(dst + 32 * c + x, d[x]);
+                    for (int x = 0; x < 32; x += 4)
+                        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 32 * c + x),
+                                     "f"(d[x]), "f"(d[x + 1]), "f"(d[x + 2]), "f"(d[x + 3])
+                                     : "memory");
                 }
             }
             if (GROUPED) z[(slot * H + head) * kD + f] = zsum;
@@ -503,9 +508,12 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // per sequence is more than that, g = max(kMinGroup, ceil(H total / sms)).
 // Either way the group count is at most floor(sms / H) + n_seqs.
 // group_off[s] = first group of sequence s, group_off[n_seqs] = the number of
-// groups, group_off[n_seqs + 1] = the group size.
+// groups, group_off[n_seqs + 1] = the group size.  Also zeroes the fused
+// apply's hand-off counters.
 __global__ void __launch_bounds__(1024)
-group_plan_kernel(const char* __restrict__ ws, int sms, int H, int* __restrict__ group_off) {
+group_plan_kernel(const char* __restrict__ ws, int sms, int H, int* __restrict__ group_off, int* __restrict__ counters,
+                  int n_counters) {
+    for (int x = threadIdx.x; x < n_counters; x += blockDim.x) counters[x] = 0;  // the fused form's hand-off counts
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
     const int n_seqs = hdr->status == GDN_OK ? hdr->n_seqs : 0;
     PlanLayout L(hdr->n_seqs);
@@ -514,9 +522,11 @@ group_plan_kernel(const char* __restrict__ ws, int sms, int H, int* __restrict__
     __shared__ int s_carry;
     __shared__ int s_red[2][32];
     const int tid = threadIdx.x;
-    // this thread's sequences' chunk counts (the first 8 x 1024 kept in registers)
+    // this thread's sequences' chunk counts (the first 8 x 1024 kept in registers;
+    // only the entries that exist are divided below)
     constexpr int kKeep = 8;
     int cnt[kKeep];
+    const int mine = tid < n_seqs ? (n_seqs - 1 - tid) / 1024 + 1 : 0;  // sequences tid, tid + 1024, ...
 #pragma unroll
     for (int k = 0; k < kKeep; ++k) {
         const int i = tid + 1024 * k;
@@ -528,7 +538,8 @@ group_plan_kernel(const char* __restrict__ ws, int sms, int H, int* __restrict__
     auto groups_of = [&](int g) -> int {
         int c = 0;
 #pragma unroll
-        for (int k = 0; k < kKeep; ++k) c += (cnt[k] + g - 1) / g;
+        for (int k = 0; k < kKeep; ++k)
+            if (k < mine) c += (cnt[k] + g - 1) / g;
         for (int i = tid + 1024 * kKeep; i < n_seqs; i += 1024) c += (chunk_off[i + 1] - chunk_off[i] + g - 1) / g;
         c = __reduce_add_sync(0xffffffffu, c);
         if ((tid & 31) == 0) s_red[flip][tid >> 5] = c;
@@ -681,11 +692,51 @@ constexpr uint32_t kGIdS = tc::idesc_bf16(128, 128, true, true);    // A = v^T, 
 constexpr uint32_t kGIdQ = tc::idesc_bf16(64, kGN, false, false);   // A = q, B = [h_c^T ; z_c] (both K-major)
 constexpr uint32_t kGIdV = tc::idesc_bf16(64, kGN, false, true);    // A = P (K-major), B = [v | 1] (MN-major)
 
+// Cross-CTA counters of the fused form (gpu scope).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void add_release_gpu(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded wait of one thread until *p >= target (the fused form's hand-offs
+// between the CTAs of one (sequence, head); all of them are resident at once).
+__device__ __noinline__ bool wait_count(const int* p, int target, char* ws, volatile int* abort_flag, int site) {
+    const int limit = abort_flag[1];
+    for (int it = 0;; ++it) {
+        if (*abort_flag) return false;
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (it >= limit) break;
+        __nanosleep(128);
+    }
+    WsHeader* h = reinterpret_cast<WsHeader*>(ws);
+    atomicExch(&h->status, GDN_ERR_TIMEOUT);
+    atomicCAS(&h->timeout_site, 0, site);
+    *abort_flag = 1;
+    return false;
+}
+
+// FUSED = false: CTA (g, head) applies group g from hs[g], zs[g] (kv_reduce_kernel<true>
+//   and group_scan_kernel ran before).
+// FUSED = true: one cooperative launch of `sms` CTAs, CTA b taking group b / H of
+//   head b % H, when every (sequence, head) has its groups resident at once.
+//   Phase 1: the group's K^T V (in S) and key sums, published to Sg[g][head],
+//   zg[g][head]; phase 2: once every group of the (sequence, head) has published,
+//   CTA j of them forms the prefix over the groups for its slice of the 128 x 128
+//   entries (hs, and h_T from the total; CTA 0 the key sums zs, z_T); phase 3:
+//   once every slice is done, the apply as above, its loads already in flight
+//   (the TMA warp streams the phase-1 k, v and then the phase-3 q, k, v through
+//   the same ring).  Idle CTAs first copy h0 to h_T for empty sequences.
+template <bool FUSED>
 __global__ void __launch_bounds__(kGThreads, 1)
 group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, int H,
-                   char* __restrict__ ws, const int* __restrict__ group_off, const float* __restrict__ hs,
-                   const float* __restrict__ zs, int normalize, __nv_bfloat16* __restrict__ o) {
+                   char* __restrict__ ws, const int* __restrict__ group_off, float* __restrict__ hs,
+                   float* __restrict__ zs, int normalize, __nv_bfloat16* __restrict__ o, int* __restrict__ counters,
+                   float* __restrict__ Sg, float* __restrict__ zg, const float* __restrict__ h0,
+                   float* __restrict__ h_T, float* __restrict__ z_T) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -693,14 +744,33 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     char* const sptr = reinterpret_cast<char*>(smem_raw) + pad;
     const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
     if (hdr->status != GDN_OK) return;
-    const int n_seqs = hdr->n_seqs, head = blockIdx.y, g = blockIdx.x;
-    if (g >= group_off[n_seqs]) return;
+    const int n_seqs = hdr->n_seqs;
     PlanLayout L(n_seqs);
     const int* cu = reinterpret_cast<const int*>(ws + L.cu);
     const int* chunk_off = reinterpret_cast<const int*>(ws + L.chunk_off);
+    int head, g;
+    if (FUSED) {
+        // empty sequences have no group: their final state is h0, their key sum zero
+        for (int u = blockIdx.x; u < n_seqs * H; u += gridDim.x) {
+            const int sq = u / H;
+            if (chunk_off[sq + 1] != chunk_off[sq]) continue;
+            if (h_T)
+                for (int x = threadIdx.x; x < kD * kD; x += blockDim.x)
+                    h_T[(size_t)u * kD * kD + x] = h0 ? h0[(size_t)u * kD * kD + x] : 0.f;
+            if (z_T && threadIdx.x < kD) z_T[(size_t)u * kD + threadIdx.x] = 0.f;
+        }
+        if ((int)blockIdx.x >= group_off[n_seqs] * H) return;
+        head = blockIdx.x % H;
+        g = blockIdx.x / H;
+    } else {
+        head = blockIdx.y;
+        g = blockIdx.x;
+        if (g >= group_off[n_seqs]) return;
+    }
     int gseq, c0, nc;
     group_range(group_off, chunk_off, n_seqs, group_off[n_seqs + 1], g, gseq, c0, nc);
     if (nc == 0) return;
+    const int n1 = FUSED ? nc : 0;  // phase-1 loads before the apply's
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     auto bar = [&](int i) { return sbase + kGBarOff + 8u * (uint32_t)i; };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + kGBarOff + 112);
@@ -724,38 +794,58 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t tmem = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t*>(sptr + kGBarOff + 120), 0);
 
     if (warp == 0) {
-        // ---- TMA: q, k, v of the group's chunks into stage i % kGStages
+        // ---- TMA: load l (phase-1 k, v for l < n1, then q, k, v of chunk l - n1) into stage l % kGStages
         int issued = 0;
         if (lane == 0) {
-            for (int i = 0; i < nc; ++i) {
-                const int s = i % kGStages;
-                if (i >= kGStages && !lv_wait(bar(G_EMPTY + s), ((i / kGStages) - 1) & 1, ws, abort_flag, 4300)) break;
-                const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
+            for (int l = 0; l < n1 + nc; ++l) {
+                const int s = l % kGStages;
+                if (l >= kGStages && !lv_wait(bar(G_EMPTY + s), ((l / kGStages) - 1) & 1, ws, abort_flag, 4300)) break;
+                const bool apply = l >= n1;
+                const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + (apply ? l - n1 : l));
                 const uint32_t st = sbase + s * kGStage;
-                tc::mbar_arrive_expect_tx(bar(G_FULL + s), 49152);
-                tc::tma_load_3d(st, &tm_q, 0, head, r.t0, bar(G_FULL + s));
-                tc::tma_load_3d(st + 8192, &tm_q, 64, head, r.t0, bar(G_FULL + s));
+                tc::mbar_arrive_expect_tx(bar(G_FULL + s), apply ? 49152 : 32768);
+                if (apply) {
+                    tc::tma_load_3d(st, &tm_q, 0, head, r.t0, bar(G_FULL + s));
+                    tc::tma_load_3d(st + 8192, &tm_q, 64, head, r.t0, bar(G_FULL + s));
+                }
                 tc::tma_load_3d(st + 16384, &tm_k, 0, head, r.t0, bar(G_FULL + s));
                 tc::tma_load_3d(st + 24576, &tm_k, 64, head, r.t0, bar(G_FULL + s));
                 tc::tma_load_3d(st + 32768, &tm_v, 0, head, r.t0, bar(G_FULL + s));
                 tc::tma_load_3d(st + 40960, &tm_v, 64, head, r.t0, bar(G_FULL + s));
-                issued = i + 1;
+                issued = l + 1;
             }
             if (*abort_flag)
-                for (int i = max(0, issued - kGStages); i < issued; ++i)
-                    tc::mbar_wait(bar(G_FULL + i % kGStages), (i / kGStages) & 1);
+                for (int l = max(0, issued - kGStages); l < issued; ++l)
+                    tc::mbar_wait(bar(G_FULL + l % kGStages), (l / kGStages) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---- MMA, chunk by chunk
+        // ---- MMA
         int npart = 0;
+        // phase 1: S = sum over the group's chunks of v^T k
+        for (int l = 0; l < n1; ++l) {
+            const int s = l % kGStages;
+            const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + l);
+            const uint32_t st = sbase + s * kGStage, k0 = st + 16384, v0 = st + 32768;
+            if (!warp_wait(bar(G_FULL + s), (l / kGStages) & 1, ws, abort_flag, 4310)) break;
+            if (r.n < kChunk) {
+                if (!warp_wait(bar(G_ZREADY), npart & 1, ws, abort_flag, 4311)) break;
+                ++npart;
+            }
+            tc::tc_fence_after();
+            tc::mma_ss_n<4>(tmem + kTS32, tc::sdesc(v0, 8192, 1024), 128, tc::sdesc(k0, 8192, 1024), 128, kGIdS, l > 0);
+            tc::commit_e(bar(G_EMPTY + s));
+        }
+        if (FUSED) tc::commit_e(bar(G_SD));  // phase 1 done: the state group may read S (phase 0 of G_SD)
+        const int sd0 = FUSED ? 1 : 0;        // G_SD phases taken before the apply's
+        // the apply, chunk by chunk
         for (int i = 0; i < nc; ++i) {
-            const int s = i % kGStages, b = i & 1;
+            const int l = n1 + i, s = l % kGStages, b = i & 1;
             const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
             const uint32_t st = sbase + s * kGStage, q0 = st, k0 = st + 16384, v0 = st + 32768;
             const uint32_t snap = sbase + kGSnap + 2 * kGSnapBox * (uint32_t)b;
             const uint32_t dO = tmem + (b ? kTO1 : kTO0);
-            if (!warp_wait(bar(G_FULL + s), (i / kGStages) & 1, ws, abort_flag, 4301)) break;
+            if (!warp_wait(bar(G_FULL + s), (l / kGStages) & 1, ws, abort_flag, 4301)) break;
             if (r.n < kChunk) {  // the state group first zeroes the rows past the sequence's end
                 if (!warp_wait(bar(G_ZREADY), npart & 1, ws, abort_flag, 4302)) break;
                 ++npart;
@@ -784,12 +874,14 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc::commit_e(bar(G_OD + b));
             tc::commit_e(bar(G_EMPTY + s));
         }
+        (void)sd0;
         tc::commit_e(bar(G_FIN));
         __syncwarp();
     } else if (warp < 6) {
         // ---- state group: thread f owns state row j = f (a TMEM lane) and key-sum entry z[f]
         const int f = 32 * (warp & 3) + lane;
         const bool leader = warp == 2 && lane == 0;
+        const int sd0 = FUSED ? 1 : 0;  // G_SD phases taken before the apply's
         // row f of a snapshot half from 64 fp32 values (columns 64 half .. 64 half + 63)
         auto snap_half = [&](uint32_t snap, int half, const float (&x)[64]) {
 #pragma unroll
@@ -807,6 +899,17 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             asm volatile("st.shared.u16 [%0], %1;" ::"r"(tc::sw128(box, 128, c) + e), "h"(__bfloat16_as_ushort(hi)) : "memory");
             asm volatile("st.shared.u16 [%0], %1;" ::"r"(tc::sw128(box, 129, c) + e), "h"(__bfloat16_as_ushort(lo)) : "memory");
         };
+        // rows past a partial chunk's end belong to the next sequence: zero them in k and v
+        auto zero_tail = [&](uint32_t st, int n) {
+            for (int x = f; x < (kChunk - n) * 32; x += 128) {
+                const int t = n + (x >> 5), c32 = x & 31;  // 16-byte chunk c32 of k (0..15) or v (16..31)
+                const uint32_t base = st + 16384 + (c32 < 16 ? 0u : 16384u) + (uint32_t)((c32 & 15) >> 3) * 8192;
+                tc::st_shared_v4(tc::sw128(base, t, c32 & 7), 0u, 0u, 0u, 0u);
+            }
+            tc::fence_proxy_async();
+            tc::named_bar(1, 128);
+            if (leader) tc::mbar_arrive(bar(G_ZREADY));
+        };
         // fixed parts: the ones column after v in both stages (row s, column 0 of the
         // third box), rows 128..135 of both snapshots zero
         for (int x = f; x < kGStages * 64 * 8; x += 128) {
@@ -819,14 +922,89 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc::st_shared_v4(sbase + kGSnap + (uint32_t)box * kGSnapBox + (uint32_t)row * 128 + (uint32_t)c * 16, 0u,
                              0u, 0u, 0u);
         }
-        float zf = 0.f;
-        {  // S and the first snapshot from the group's starting state (h[i][j] -> S[j][i])
+        bool ok = true;
+        if (FUSED) {
+            // ---- phase 1: the group's key sums (the MMA warp sums v^T k into S)
+            const bool need_z = normalize || z_T != nullptr;
+            float zred = 0.f;
+            for (int l = 0; l < n1 && ok; ++l) {
+                const int s = l % kGStages;
+                const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + l);
+                const uint32_t st = sbase + s * kGStage;
+                if (!(ok = group_wait(leader, 1, bar(G_FULL + s), (l / kGStages) & 1, ws, abort_flag, 4312))) break;
+                if (r.n < kChunk) zero_tail(st, r.n);
+                if (need_z) zred += key_column_sum(st + 16384, f, r.n);
+                tc::named_bar(1, 128);
+                if (leader) tc::mbar_arrive(bar(G_EMPTY + s));
+            }
+            const int u = gseq * H + head, jg = g - group_off[gseq], ng = group_off[gseq + 1] - group_off[gseq];
+            const size_t gb = (size_t)group_off[gseq];
+            if (ok) ok = group_wait(leader, 1, bar(G_SD), 0, ws, abort_flag, 4313);
+            if (ok) {
+                // publish this group's sum (h layout [i][j]: row i, entry j = f) and key sums
+                tc::tc_fence_after();
+                float* dst = Sg + ((size_t)g * H + head) * kD * kD + f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    float x[32];
+                    tc::tmem_ld32(tmem + lane_off + kTS32 + 32 * c, x);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) dst[(size_t)(32 * c + e) * kD] = x[e];
+                }
+                zg[((size_t)g * H + head) * kD + f] = zred;
+                __threadfence();
+                tc::tc_fence_before();
+                tc::named_bar(1, 128);
+                if (leader) add_release_gpu(counters + u, 1);
+                // ---- phase 2: once all groups of (sequence, head) published, this CTA's slice of the prefix
+                bool got = true;
+                if (leader) got = wait_count(counters + u, ng, ws, abort_flag, 4314);
+                ok = tc::named_bar_and(1, 128, got);
+            }
+            if (ok) {
+                const int per = ((kD * kD / ng) + 3) & ~3;
+                const int e0 = min(kD * kD, jg * per), e1 = min(kD * kD, e0 + per);
+                const size_t ub = (size_t)u * kD * kD;
+                for (int e = e0 + 4 * f; e < e1; e += 4 * 128) {
+                    float4 acc = h0 ? *reinterpret_cast<const float4*>(h0 + ub + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int gg = 0; gg < ng; ++gg) {  // (L2 loads: other CTAs of this launch wrote Sg)
+                        const size_t at = ((gb + gg) * H + head) * kD * kD + e;
+                        const float4 d = __ldcg(reinterpret_cast<const float4*>(Sg + at));
+                        *reinterpret_cast<float4*>(hs + at) = acc;
+                        acc.x += d.x;
+                        acc.y += d.y;
+                        acc.z += d.z;
+                        acc.w += d.w;
+                    }
+                    if (h_T) *reinterpret_cast<float4*>(h_T + ub + e) = acc;
+                }
+                if (jg == 0) {
+                    float zacc = 0.f;
+                    for (int gg = 0; gg < ng; ++gg) {
+                        const size_t at = ((gb + gg) * H + head) * kD + f;
+                        const float d = __ldcg(zg + at);
+                        zs[at] = zacc;
+                        zacc += d;
+                    }
+                    if (z_T) z_T[(size_t)u * kD + f] = zacc;
+                }
+                __threadfence();
+                tc::named_bar(1, 128);
+                if (leader) add_release_gpu(counters + n_seqs * H + u, 1);
+                bool got = true;
+                if (leader) got = wait_count(counters + n_seqs * H + u, ng, ws, abort_flag, 4315);
+                ok = tc::named_bar_and(1, 128, got);
+            }
+        }
+        if (ok) {  // S and the first snapshot from the group's starting state (h[i][j] -> S[j][i])
+            float zf = 0.f;
             const float* hsrc = hs + ((size_t)g * H + head) * kD * kD;
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 float x[64];
 #pragma unroll
-                for (int i2 = 0; i2 < 64; ++i2) x[i2] = hsrc[(size_t)(64 * half + i2) * kD + f];
+                for (int i2 = 0; i2 < 64; ++i2) x[i2] = __ldcg(hsrc + (size_t)(64 * half + i2) * kD + f);
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
                     uint32_t r[16];
@@ -839,59 +1017,50 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc::tmem_wait_st();
             tc::named_bar(1, 128);  // rows 128..135 were zeroed by other threads: the z rows come after
             if (normalize) {
-                zf = zs[((size_t)g * H + head) * kD + f];
+                zf = __ldcg(zs + ((size_t)g * H + head) * kD + f);
                 snap_z(sbase + kGSnap, zf);
             }
             tc::fence_proxy_async();
             tc::tc_fence_before();
             tc::named_bar(1, 128);
             if (leader) tc::mbar_arrive(bar(G_SNAP));
-        }
-        for (int i = 0; i < nc; ++i) {
-            const int s = i % kGStages;
-            const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
-            const uint32_t st = sbase + s * kGStage, k0 = st + 16384;
-            if (!group_wait(leader, 1, bar(G_FULL + s), (i / kGStages) & 1, ws, abort_flag, 4306)) break;
-            if (r.n < kChunk) {  // rows past a partial chunk's end belong to the next sequence: zero them in k and v
-                for (int x = f; x < (kChunk - r.n) * 32; x += 128) {
-                    const int t = r.n + (x >> 5), c32 = x & 31;  // 16-byte chunk c32 of k (0..15) or v (16..31)
-                    const uint32_t base = (c32 < 16 ? k0 : st + 32768) + (uint32_t)((c32 & 15) >> 3) * 8192;
-                    tc::st_shared_v4(tc::sw128(base, t, c32 & 7), 0u, 0u, 0u, 0u);
-                }
-                tc::fence_proxy_async();
-                tc::named_bar(1, 128);
-                if (leader) tc::mbar_arrive(bar(G_ZREADY));
-            }
-            const float zc = normalize ? key_column_sum(k0, f, r.n) : 0.f;
-            if (i + 1 < nc) {
-                // the state after this chunk, for the next one
-                if (!group_wait(leader, 1, bar(G_SD), i & 1, ws, abort_flag, 4307)) break;
-                tc::tc_fence_after();
-                const uint32_t snap = sbase + kGSnap + 2 * kGSnapBox * (uint32_t)((i + 1) & 1);
+            for (int i = 0; i < nc; ++i) {
+                const int l = n1 + i, s = l % kGStages;
+                const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
+                const uint32_t st = sbase + s * kGStage, k0 = st + 16384;
+                if (!group_wait(leader, 1, bar(G_FULL + s), (l / kGStages) & 1, ws, abort_flag, 4306)) break;
+                if (r.n < kChunk) zero_tail(st, r.n);
+                const float zc = normalize ? key_column_sum(k0, f, r.n) : 0.f;
+                if (i + 1 < nc) {
+                    // the state after this chunk, for the next one
+                    if (!group_wait(leader, 1, bar(G_SD), (sd0 + i) & 1, ws, abort_flag, 4307)) break;
+                    tc::tc_fence_after();
+                    const uint32_t snap = sbase + kGSnap + 2 * kGSnapBox * (uint32_t)((i + 1) & 1);
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float x[64], y[32];
-                    tc::tmem_ld32(tmem + lane_off + kTS32 + 64 * half, y);
-                    tc::tmem_ld32(tmem + lane_off + kTS32 + 64 * half + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-                    tc::tmem_wait_ld();
+                    for (int half = 0; half < 2; ++half) {
+                        float x[64], y[32];
+                        tc::tmem_ld32(tmem + lane_off + kTS32 + 64 * half, y);
+                        tc::tmem_ld32(tmem + lane_off + kTS32 + 64 * half + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+                        tc::tmem_wait_ld();
 #pragma unroll
-                    for (int e2 = 0; e2 < 32; ++e2) x[e2] = y[e2];
-                    snap_half(snap, half, x);
+                        for (int e2 = 0; e2 < 32; ++e2) x[e2] = y[e2];
+                        snap_half(snap, half, x);
+                    }
+                    if (normalize) {
+                        zf += zc;
+                        snap_z(snap, zf);
+                    }
+                    tc::fence_proxy_async();
+                    tc::tc_fence_before();
+                    tc::named_bar(1, 128);
+                    if (leader) {
+                        tc::mbar_arrive(bar(G_SNAP));
+                        tc::mbar_arrive(bar(G_EMPTY + s));
+                    }
+                } else {
+                    tc::named_bar(1, 128);
+                    if (leader) tc::mbar_arrive(bar(G_EMPTY + s));
                 }
-                if (normalize) {
-                    zf += zc;
-                    snap_z(snap, zf);
-                }
-                tc::fence_proxy_async();
-                tc::tc_fence_before();
-                tc::named_bar(1, 128);
-                if (leader) {
-                    tc::mbar_arrive(bar(G_SNAP));
-                    tc::mbar_arrive(bar(G_EMPTY + s));
-                }
-            } else {
-                tc::named_bar(1, 128);
-                if (leader) tc::mbar_arrive(bar(G_EMPTY + s));
             }
         }
     } else if (warp < 10) {
@@ -1049,14 +1218,31 @@ static long long max_groups(int H, int n_seqs) {
     return sms / (H > 0 ? H : 1) + n_seqs;
 }
 
+// The one-launch form needs every group resident at once: true when even one
+// group per (sequence, head) fits the SMs, which the group size search then
+// guarantees for all of them.  It pays for small problems (measured on B300:
+// ahead up to ~30 chunks of 64 tokens per SM and head, behind from ~55, where
+// the separate sum kernel's two CTAs per SM win), so it is taken up to 40.
+// GDN_LINEAR_GROUPED_FORM=fused or =unfused overrides the size rule (fused
+// still only where it can run).
+static bool grouped_fused(const PrefillArgs& a) {
+    const long long sms = sm_count() > 0 ? sm_count() : 148;
+    if (a.T_total <= 0 || (long long)a.H * a.n_seqs > sms) return false;
+    const char* f = getenv("GDN_LINEAR_GROUPED_FORM");
+    if (f != nullptr && strcmp(f, "fused") == 0) return true;
+    if (f != nullptr && strcmp(f, "unfused") == 0) return false;
+    return (long long)max_chunks(a.T_total, a.n_seqs) * a.H <= 40 * sms;
+}
+
 size_t linear_grouped_extra_bytes(int64_t T, int H, int n_seqs) {
     (void)T;
     const size_t ng = (size_t)max_groups(H, n_seqs);
     // group_off, the half-group sums Sg (2 per group), the starting states hs,
-    // the half-group key sums zg (2 per group), the starting key sums zs
+    // the half-group key sums zg (2 per group), the starting key sums zs, the
+    // fused form's two counters per (sequence, head)
     return align256(sizeof(int) * (size_t)(n_seqs + 2)) + align256(sizeof(float) * 2 * ng * H * linvar::kD * linvar::kD) +
            align256(sizeof(float) * ng * H * linvar::kD * linvar::kD) + align256(sizeof(float) * 2 * ng * H * linvar::kD) +
-           align256(sizeof(float) * ng * H * linvar::kD);
+           align256(sizeof(float) * ng * H * linvar::kD) + align256(sizeof(int) * 2 * (size_t)n_seqs * H);
 }
 
 cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* extra, bool normalize, float* h_T,
@@ -1073,8 +1259,11 @@ cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* ext
     float* zg = reinterpret_cast<float*>(p);
     p += align256(sizeof(float) * 2 * ng * a.H * kD);
     float* zs = reinterpret_cast<float*>(p);
+    p += align256(sizeof(float) * ng * a.H * kD);
+    int* counters = reinterpret_cast<int*>(p);
     if (a.n_seqs == 0) return cudaSuccess;
-    group_plan_kernel<<<1, 1024, 0, st>>>(plan_ws, sms, a.H, group_off);
+    const bool fused = grouped_fused(a);
+    group_plan_kernel<<<1, 1024, 0, st>>>(plan_ws, sms, a.H, group_off, counters, fused ? 2 * a.n_seqs * a.H : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (a.T_total > 0) {
@@ -1082,23 +1271,37 @@ cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* ext
         if (!encode_token_map(&mq, a.q, a.T_total, a.H) || !encode_token_map(&mk, a.k, a.T_total, a.H) ||
             !encode_token_map(&mv, a.v, a.T_total, a.H) || !encode_token_map(&mo, a.o, a.T_total, a.H))
             return cudaErrorInvalidValue;
+        __nv_bfloat16* o = (__nv_bfloat16*)a.o;
+        const int nrm = normalize ? 1 : 0;
+        if (fused) {
+            e = cudaFuncSetAttribute(group_apply_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+            if (e != cudaSuccess) return e;
+            int H = a.H;
+            char* ws = plan_ws;
+            const float* h0 = a.h0;
+            void* args[] = {&mq, &mk, &mv, &mo, &H, &ws, &group_off, &hs, &zs, (void*)&nrm, &o, &counters, &Sg, &zg,
+                            (void*)&h0, &h_T, &z_T};
+            return cudaLaunchCooperativeKernel((const void*)group_apply_kernel<true>, dim3((unsigned)sms),
+                                               dim3(kGThreads), args, kGSmem, st);
+        }
         e = cudaFuncSetAttribute(kv_reduce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmem);
         if (e != cudaSuccess) return e;
         kv_reduce_kernel<true><<<dim3((unsigned)(2 * ng), a.H), kLvThreads, kRSmem, st>>>(mk, mv, a.H, 0, plan_ws,
-                                                                                   group_off, Sg, zg);
+                                                                                         group_off, Sg, zg);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / kScanCols), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0, Sg,
-                                                                                 zg, hs, zs, h_T, z_T);
+        group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / kScanCols), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0,
+                                                                                       Sg, zg, hs, zs, h_T, z_T);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(group_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+        e = cudaFuncSetAttribute(group_apply_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
         if (e != cudaSuccess) return e;
-        group_apply_kernel<<<dim3((unsigned)ng, a.H), kGThreads, kGSmem, st>>>(
-            mq, mk, mv, mo, a.H, plan_ws, group_off, hs, zs, normalize ? 1 : 0, (__nv_bfloat16*)a.o);
+        group_apply_kernel<false><<<dim3((unsigned)ng, a.H), kGThreads, kGSmem, st>>>(
+            mq, mk, mv, mo, a.H, plan_ws, group_off, hs, zs, nrm, o, nullptr, nullptr, nullptr, nullptr, nullptr,
+            nullptr);
         return cudaGetLastError();
     }
     // no tokens: every final state is its initial state, every key sum zero
-    group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / kScanCols), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0, Sg, zg,
-                                                                             hs, zs, h_T, z_T);
+    group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / kScanCols), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0, Sg,
+                                                                                   zg, hs, zs, h_T, z_T);
     return cudaGetLastError();
 }
 

@@ -465,16 +465,19 @@ def test_linear_bidirectional_forced_timeout_then_recovery(g):
 
 # ------------------------------------------------------------------ causal linear attention, grouped
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("lengths,H,h0_std", [([1, 100, 0, 257, 64, 700], 4, 0.5), ([3000, 1500], 8, 0.0),
                                               ([64, 65, 63, 128, 1], 4, 0.1)])
-def test_linear_grouped_against_oracle(g, monkeypatch, lengths, H, h0_std):
+def test_linear_grouped_against_oracle(g, monkeypatch, lengths, H, h0_std, fused):
     """Causal linear attention through groups of chunks (the default path of
-    linear_attn_fwd for bf16, d = 128): ragged sequences, several groups per
-    sequence, partial and empty chunks, with and without h0; every output and
-    every final state against the oracle's recurrence."""
+    linear_attn_fwd for bf16, d = 128), in one cooperative launch (fused) and
+    as separate sum, prefix and apply kernels: ragged sequences, several
+    groups per sequence, partial and empty chunks, with and without h0; every
+    output and every final state against the oracle's recurrence."""
     monkeypatch.delenv("GDN_LINEAR_PATH", raising=False)
     monkeypatch.delenv("GDN_PREFILL_PAIR", raising=False)
     monkeypatch.delenv("GDN_TWO_LEVEL", raising=False)
+    monkeypatch.setenv("GDN_LINEAR_GROUPED_FORM", "fused" if fused else "unfused")
     inp = gi.linear_inputs(lengths, H, 128, 128, "bf16", h0_std=h0_std, seed=61)
     d = dev(inp)
     o, hT, ws = g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"])
@@ -517,8 +520,10 @@ def test_linear_grouped_t131072_h32(g, monkeypatch):
     assert rel(hT, inp["h0"].double().numpy() + rkv) <= TOL["bf16"]
 
 
-def test_linear_grouped_forced_timeout_then_recovery(g, monkeypatch):
+@pytest.mark.parametrize("fused", [True, False])
+def test_linear_grouped_forced_timeout_then_recovery(g, monkeypatch, fused):
     monkeypatch.delenv("GDN_LINEAR_PATH", raising=False)
+    monkeypatch.setenv("GDN_LINEAR_GROUPED_FORM", "fused" if fused else "unfused")
     inp = gi.linear_inputs([700, 300], 4, 128, 128, "bf16", h0_std=0.1, seed=63)
     d = dev(inp)
     args = [d[k] for k in ("q", "k", "v", "h0", "cu_seqlens")]
