@@ -158,7 +158,16 @@ GDN_API gdn_status gdn_chunk_fwd_block_adjacent(const void *q, const void *k, co
  * ("Как ускорить LLM на длинном контексте", section "Linear attention"; the
  * reassociated evaluation order of "За пределами self-attention", section
  * "Линейное внимание…").  No gates, no delta term, no normaliser, causal.
- * Same layouts and rules as gdn_chunk_fwd.
+ * Same layouts and rules as gdn_chunk_fwd.  For bf16 with dk = dv = 128 the
+ * chain is cut into groups of chunks: each group's sum of k^T v, a prefix over
+ * the groups (h0 first) for each group's starting state, then every group's
+ * outputs from its own start, all groups side by side.  Small calls (every
+ * (sequence, head) resident, at most 40 chunks per SM) do this in one
+ * cooperative launch whose CTAs hand their sums to each other through
+ * bounded waits on counters in the workspace.  The result equals the
+ * sequential evaluation up to rounding.  GDN_LINEAR_GROUPED_FORM=fused or
+ * =unfused overrides the size rule; GDN_LINEAR_PATH=cluster runs the
+ * sequential kernels of gdn_chunk_fwd instead.
  */
 GDN_API size_t linear_attn_fwd_workspace_size(int64_t T_total, int H, int dk, int dv, int n_seqs,
                                       gdn_dtype io_dtype);
@@ -184,8 +193,10 @@ GDN_API gdn_status linear_attn_fwd(const void *q, const void *k, const void *v, 
  * kv [n_seqs][H][dk][dv] = sum_t k_t v_t^T over each sequence (h = S^T of the
  * final state), z [n_seqs][H][dk] = sum_t k_t.  Bidirectional calls run a
  * tcgen05 reduction of K^T V over groups of chunks and a tcgen05 apply pass;
- * causal calls run the causal prefill of linear_attn_fwd for the numerator
- * and, when normalised, a key-prefix pass that divides o.  Workspace: the
+ * causal calls run the grouped evaluation of linear_attn_fwd, whose output
+ * MMA also yields the normaliser q_t . (sum of k_s, s <= t) (the running key
+ * sum rides as extra rows of the state operand, a column of ones after v).
+ * kv and z of a causal call are the final state and key sum.  Workspace: the
  * query below; status word at its offset 0, as for the other calls.
  */
 GDN_API size_t linear_attn_variant_workspace_size(int64_t T_total, int H, int dk, int dv, int n_seqs,
