@@ -480,12 +480,13 @@ def run_workload(args):
         if kind == "bidir_norm":  # plan, K^T V reduction, apply
             bytes_per_call, launches, segs, path = 4 * Tt * Hh * D * 2, 3, 1, "linear_bidirectional"
         elif kind == "causal_norm" or (kind == "linear" and linear_grouped()):
-            # plan, group plan, then one cooperative launch (sums, prefix, apply) for small
-            # problems, else half-group K^T V sums, prefix over the groups, group apply
+            # the plan (with the group plan), then one cooperative launch (sums, prefix,
+            # apply) for small problems, else half-group K^T V sums, prefix over the
+            # groups, group apply
             sms = torch.cuda.get_device_properties(0).multi_processor_count
             form = os.environ.get("GDN_LINEAR_GROUPED_FORM", "")
             fused = Hh * nn <= sms and (form == "fused" or (form != "unfused" and (Tt // 64 + nn) * Hh <= 40 * sms))
-            launches, segs = (3 if fused else 5), 1
+            launches, segs = (2 if fused else 4), 1
             path = "linear_grouped_fused" if fused else "linear_grouped"
             if kind == "causal_norm":
                 bytes_per_call = 4 * Tt * Hh * D * 2

@@ -139,9 +139,8 @@ gdn_status prefill(const PrefillArgs& a, size_t ws_bytes, cudaStream_t st) {
     if (use_grouped_linear(a)) {
         gdn_status s = check_prefill(a, ws_bytes, grouped_linear_bytes(a.T_total, a.H, a.n_seqs), true);
         if (s != GDN_OK) return s;
-        cudaError_t e = launch_plan(a.cu_seqlens, a.n_seqs, a.T_total, g_wait_limit.load(), a.ws, st);
-        if (e == cudaSuccess)
-            e = launch_linear_grouped(a, a.ws, a.ws + align256(plan_bytes(a.n_seqs)), false, a.h_T, nullptr, st);
+        cudaError_t e = launch_linear_grouped(a, a.ws, a.ws + align256(plan_bytes(a.n_seqs)), false, a.h_T, nullptr,
+                                              g_wait_limit.load(), st);
         return cuda_status(e);
     }
     const bool pair = use_pair(a);
@@ -288,10 +287,13 @@ gdn_status linear_attn_variant_fwd(const void* q, const void* k, const void* v, 
     const int wl = g_wait_limit.load();
     char* plan = a.ws;
     char* extra = a.ws + align256(plan_bytes(n_seqs));
-    cudaError_t e = launch_plan(cu_seqlens, n_seqs, T_total, wl, plan, st);
-    if (e == cudaSuccess)
-        e = causal ? launch_linear_grouped(a, plan, extra, normalize != 0, kv, z, st)
-                   : launch_linear_bidirectional(a, plan, extra, normalize != 0, kv, z, st);
+    cudaError_t e;
+    if (causal) {
+        e = launch_linear_grouped(a, plan, extra, normalize != 0, kv, z, wl, st);
+    } else {
+        e = launch_plan(cu_seqlens, n_seqs, T_total, wl, plan, st);
+        if (e == cudaSuccess) e = launch_linear_bidirectional(a, plan, extra, normalize != 0, kv, z, st);
+    }
     return cuda_status(e);
 }
 

@@ -52,8 +52,18 @@ StagedBuffers staged_buffers(char* ws, int64_t T, int H, int dk, int dv, int n_s
 // (device, may be NULL): a status word found earlier in the same call; if it
 // is not GDN_OK the plan carries it, and the kernels reading the plan skip
 // their work.
+// The grouped causal linear attention's part of the plan (group_off NULL: none):
+// the group size and numbering, written to group_off (n_seqs + 2 ints), and
+// n_counters hand-off counters zeroed.
+struct GroupPlan {
+    int sms, H;
+    int* group_off;
+    int* counters;
+    int n_counters;
+};
+constexpr int kGroupMinChunks = 4;  // chunks per group, at least
 cudaError_t launch_plan(const int32_t* cu, int n_seqs, int64_t T_total, int wait_limit, void* ws,
-                        cudaStream_t st, const int* upstream = nullptr);
+                        cudaStream_t st, const int* upstream = nullptr, const GroupPlan* gp = nullptr);
 cudaError_t launch_kkt(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
 cudaError_t launch_wy(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
 cudaError_t launch_state_ffma(const PrefillArgs& a, const StagedBuffers& b, cudaStream_t st);
@@ -92,7 +102,8 @@ size_t linear_variant_extra_bytes(int64_t T, int H, int n_seqs, bool causal);
 cudaError_t launch_linear_bidirectional(const PrefillArgs& a, char* plan_ws, char* extra, bool normalize,
                                         float* kv_out, float* z_out, cudaStream_t st);
 size_t linear_grouped_extra_bytes(int64_t T, int H, int n_seqs);
+// Runs its own plan (with the group plan) at plan_ws.
 cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* extra, bool normalize, float* h_T,
-                                  float* z_T, cudaStream_t st);
+                                  float* z_T, int wait_limit, cudaStream_t st);
 
 }  // namespace gdn

@@ -37,7 +37,7 @@ bool encode_token_map(CUtensorMap* m, const void* ptr, int64_t T, int H);
 namespace linvar {
 
 constexpr int kD = 128;
-constexpr int kMinGroup = 4;   // chunks per reduce / apply CTA, at least
+constexpr int kMinGroup = kGroupMinChunks;  // chunks per reduce / apply CTA, at least
 
 struct ChunkRef {
     int seq, t0, n;
@@ -501,91 +501,6 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // K^T V (kv_reduce_kernel<true>) give each group's starting state by a prefix
 // (group_scan_kernel), and every group then runs its own chunks in order from
 // that state (group_apply_kernel), all groups side by side.
-
-// Picks the group size and numbers the groups.  The size is the smallest
-// g >= kMinGroup for which all (sequence, head) pairs together have at most
-// `sms` groups (one wave of one-CTA-per-SM launches), or, when even one group
-// per sequence is more than that, g = max(kMinGroup, ceil(H total / sms)).
-// Either way the group count is at most floor(sms / H) + n_seqs.
-// group_off[s] = first group of sequence s, group_off[n_seqs] = the number of
-// groups, group_off[n_seqs + 1] = the group size.  Also zeroes the fused
-// apply's hand-off counters.
-__global__ void __launch_bounds__(1024)
-group_plan_kernel(const char* __restrict__ ws, int sms, int H, int* __restrict__ group_off, int* __restrict__ counters,
-                  int n_counters) {
-    for (int x = threadIdx.x; x < n_counters; x += blockDim.x) counters[x] = 0;  // the fused form's hand-off counts
-    const WsHeader* hdr = reinterpret_cast<const WsHeader*>(ws);
-    const int n_seqs = hdr->status == GDN_OK ? hdr->n_seqs : 0;
-    PlanLayout L(hdr->n_seqs);
-    const int* chunk_off = reinterpret_cast<const int*>(ws + L.chunk_off);
-    __shared__ int s_scan[1024];
-    __shared__ int s_carry;
-    __shared__ int s_red[2][32];
-    const int tid = threadIdx.x;
-    // this thread's sequences' chunk counts (the first 8 x 1024 kept in registers;
-    // only the entries that exist are divided below)
-    constexpr int kKeep = 8;
-    int cnt[kKeep];
-    const int mine = tid < n_seqs ? (n_seqs - 1 - tid) / 1024 + 1 : 0;  // sequences tid, tid + 1024, ...
-#pragma unroll
-    for (int k = 0; k < kKeep; ++k) {
-        const int i = tid + 1024 * k;
-        cnt[k] = i < n_seqs ? chunk_off[i + 1] - chunk_off[i] : 0;
-    }
-    // number of groups of size g over all sequences (every thread gets it; the
-    // count is at most the number of chunks, which fits an int)
-    int flip = 0;
-    auto groups_of = [&](int g) -> int {
-        int c = 0;
-#pragma unroll
-        for (int k = 0; k < kKeep; ++k)
-            if (k < mine) c += (cnt[k] + g - 1) / g;
-        for (int i = tid + 1024 * kKeep; i < n_seqs; i += 1024) c += (chunk_off[i + 1] - chunk_off[i] + g - 1) / g;
-        c = __reduce_add_sync(0xffffffffu, c);
-        if ((tid & 31) == 0) s_red[flip][tid >> 5] = c;
-        __syncthreads();  // alternate buffers: one barrier per evaluation
-        int t = 0;
-#pragma unroll
-        for (int w = 0; w < 32; ++w) t += s_red[flip][w];
-        flip ^= 1;
-        return t;
-    };
-    const int total = n_seqs > 0 ? chunk_off[n_seqs] : 0;
-    int lo = kMinGroup, hi = max(kMinGroup, total);
-    int group;
-    if ((long long)H * groups_of(hi) <= sms) {
-        while (lo < hi) {  // groups_of is non-increasing in g
-            const int mid = (lo + hi) >> 1;
-            if ((long long)H * groups_of(mid) <= sms) hi = mid; else lo = mid + 1;
-        }
-        group = lo;
-    } else {
-        group = (int)max((long long)kMinGroup, ((long long)H * total + sms - 1) / sms);
-    }
-    if (tid == 0) s_carry = 0;
-    __syncthreads();
-    for (int base = 0; base < n_seqs; base += 1024) {
-        const int i = base + tid;
-        const int ng = i < n_seqs ? (chunk_off[i + 1] - chunk_off[i] + group - 1) / group : 0;
-        s_scan[tid] = ng;
-        __syncthreads();
-        for (int off = 1; off < 1024; off <<= 1) {
-            const int x = tid >= off ? s_scan[tid - off] : 0;
-            __syncthreads();
-            s_scan[tid] += x;
-            __syncthreads();
-        }
-        if (i < n_seqs) group_off[i] = s_carry + s_scan[tid] - ng;
-        __syncthreads();
-        if (tid == 1023) s_carry += s_scan[1023];
-        __syncthreads();
-    }
-    if (tid == 0) {
-        group_off[n_seqs] = s_carry;
-        group_off[n_seqs + 1] = group;
-        if (hdr->status != GDN_OK) group_off[0] = 0;
-    }
-}
 
 // Per (sequence, head, 8 state columns): each group's starting state
 // hs[g] = h0 + the K^T V of the sequence's earlier groups (fp32; group g's
@@ -1211,7 +1126,7 @@ cudaError_t launch_linear_bidirectional(const PrefillArgs& a, char* plan_ws, cha
     return e;
 }
 
-// Groups of the causal path: group_plan_kernel picks the size on the device,
+// Groups of the causal path: the plan kernel picks the size on the device,
 // with at most floor(sms / H) + n_seqs groups in all.
 static long long max_groups(int H, int n_seqs) {
     const long long sms = sm_count() > 0 ? sm_count() : 148;
@@ -1246,7 +1161,7 @@ size_t linear_grouped_extra_bytes(int64_t T, int H, int n_seqs) {
 }
 
 cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* extra, bool normalize, float* h_T,
-                                  float* z_T, cudaStream_t st) {
+                                  float* z_T, int wait_limit, cudaStream_t st) {
     using namespace linvar;
     const size_t ng = (size_t)max_groups(a.H, a.n_seqs);
     const int sms = sm_count() > 0 ? sm_count() : 148;
@@ -1261,11 +1176,10 @@ cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* ext
     float* zs = reinterpret_cast<float*>(p);
     p += align256(sizeof(float) * ng * a.H * kD);
     int* counters = reinterpret_cast<int*>(p);
-    if (a.n_seqs == 0) return cudaSuccess;
     const bool fused = grouped_fused(a);
-    group_plan_kernel<<<1, 1024, 0, st>>>(plan_ws, sms, a.H, group_off, counters, fused ? 2 * a.n_seqs * a.H : 0);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const GroupPlan gp{sms, a.H, group_off, counters, fused ? 2 * a.n_seqs * a.H : 0};
+    cudaError_t e = launch_plan(a.cu_seqlens, a.n_seqs, a.T_total, wait_limit, plan_ws, st, nullptr, &gp);
+    if (e != cudaSuccess || a.n_seqs == 0) return e;
     if (a.T_total > 0) {
         CUtensorMap mq, mk, mv, mo;
         if (!encode_token_map(&mq, a.q, a.T_total, a.H) || !encode_token_map(&mk, a.k, a.T_total, a.H) ||
