@@ -1096,11 +1096,13 @@ cudaError_t launch_linear_bidirectional(const PrefillArgs& a, char* plan_ws, cha
     const size_t z_bytes = sizeof(float) * (size_t)a.n_seqs * a.H * kD;
     cudaError_t e = cudaMemsetAsync(kv, 0, kv_bytes, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(z, 0, z_bytes, st);
-    // chunks per CTA: about two CTAs per SM in all, at least kMinGroup chunks each,
-    // so that each (sequence, head) gets few partial sums of K^T V to add up
+    // chunks per CTA: at least kMinGroup, and few enough CTAs per head that all of
+    // them fit one wave of two CTAs per SM when that is possible (a partly filled
+    // second wave would leave most SMs idle while it runs)
     const long long nch = max_chunks(a.T_total, a.n_seqs);
     const long long sms = sm_count() > 0 ? sm_count() : 148;
-    const int group = (int)max((long long)kMinGroup, (nch * a.H + 2 * sms - 1) / (2 * sms));
+    const long long per_head = max(1LL, (2 * sms) / a.H);
+    const int group = (int)max((long long)kMinGroup, (nch + per_head - 1) / per_head);
     const unsigned groups = (unsigned)((nch + group - 1) / group);
     if (e == cudaSuccess && groups > 0 && a.T_total > 0) {
         CUtensorMap mq, mk, mv, mo;
