@@ -579,33 +579,53 @@ group_scan_kernel(const char* __restrict__ ws, const int* __restrict__ group_off
 // where the state group copies S (the state at the chunk's start) to shared
 // memory in bf16 before the chunk's S update, as a K-major [j][i] tile whose
 // rows 128 and 129 hold the running key sum z_c split into a bf16 high and low
-// part, and every stage carries a fixed column of ones after v.  So O[t][0..127]
-// is the numerator and O[t][128] + O[t][129] the normaliser
-// q_t . z_c + sum_{s <= t} q_t . k_s.  The output group divides (when
-// normalised) and stores o.  Token t of an M = 64 result sits in TMEM lane
+// part, and P times a fixed column of ones (O[t][128] += sum_s P[t][s]) adds the
+// row sums of P.  So O[t][0..127] is the numerator and
+// O[t][128] + O[t][129] the normaliser q_t . z_c + sum_{s <= t} q_t . k_s.  The
+// output group divides (when normalised) and stores o.  Shared memory holds
+// either (the one-launch form, whose small groups are bound by load latency) a
+// three-stage ring for q, k, v with one state copy and one o staging tile (the
+// next copy waits for the MMA that reads the current one) and the ones in a
+// separate 64 x 8 tile (its own N = 8 MMA), or (the large problems of the
+// separate-kernel form, bound by HBM) two stages, each with the ones as a third
+// box after v (one N = 136 MMA), and the state copy and the staging tile
+// double-buffered.  Token t of an M = 64 result sits in TMEM lane
 // 32 (t / 16) + t % 16: lanes 0..15 of each warp of the P and output groups.
 constexpr int kGThreads = 448;
-constexpr int kGStages = 2;
-constexpr uint32_t kGStage = 57344;    // q box0 | q box1 | k box0 | k box1 | v box0 | v box1 | ones
 constexpr uint32_t kGSnapBox = 17408;  // 136 rows x 128 B: one 64-column half of [h_c^T ; z_c]
-constexpr uint32_t kGSnap = kGStages * kGStage;  // two snapshots, two halves each
-constexpr uint32_t kGP = kGSnap + 4 * kGSnapBox;  // P, bf16 [t][s]
-constexpr uint32_t kGO = kGP + 8192;              // two o staging tiles, [t][j], two boxes each
-constexpr uint32_t kGBarOff = kGO + 2 * 16384;
-enum {
-    G_FULL = 0, G_EMPTY = 2, G_ZREADY = 4, G_PD = 5, G_PREADY = 6, G_SNAP = 7, G_SD = 8, G_OD = 9, G_OFREE = 11,
-    G_FIN = 13, G_COUNT = 14
+template <bool ONE_LAUNCH>
+struct GLayout {
+    static constexpr int kStages = ONE_LAUNCH ? 3 : 2;
+    static constexpr int kCopies = ONE_LAUNCH ? 1 : 2;  // state copies (two halves each)
+    static constexpr int kOTiles = ONE_LAUNCH ? 1 : 2;  // o staging tiles
+    static constexpr bool kOnesInStage = !ONE_LAUNCH;   // the ones as a third box after v in each stage
+    // stage: q box0 | q box1 | k box0 | k box1 | v box0 | v box1 [| ones]
+    static constexpr uint32_t kStage = kOnesInStage ? 57344 : 49152;
+    static constexpr uint32_t kSnap = kStages * kStage;
+    static constexpr uint32_t kP = kSnap + kCopies * 2 * kGSnapBox;  // P, bf16 [t][s]
+    static constexpr uint32_t kOnes = kP + 8192;                     // [s][8], ones in column 0 (one SW128 box)
+    static constexpr uint32_t kO = kOnes + (kOnesInStage ? 0 : 8192);  // o staging, [t][j], two boxes per tile
+    static constexpr uint32_t kBarOff = kO + kOTiles * 16384;
+    static constexpr uint32_t kSmem = kBarOff + 256 + 1024;
 };
-constexpr uint32_t kGSmem = kGBarOff + 128 + 1024;
-static_assert(kGSmem <= 232448, "group apply shared memory");
-static_assert(8 * G_COUNT <= 112, "group apply barriers");
+static_assert(GLayout<true>::kSmem <= 232448 && GLayout<false>::kSmem <= 232448, "group apply shared memory");
+// barriers (room for three stages); G_SD: the state copy may be rewritten (S
+// updated, and with one copy also read by the output MMA)
+enum {
+    G_FULL = 0, G_EMPTY = 3, G_ZREADY = 6, G_PD = 7, G_PREADY = 8, G_SNAP = 9, G_SD = 10, G_OD = 11, G_OFREE = 13,
+    G_FIN = 15, G_COUNT = 16
+};
+constexpr uint32_t kGFlag = 128, kGSlot = 136;  // abort flag and bound; TMEM address (offsets from kBarOff)
+static_assert(8 * G_COUNT <= kGFlag, "group apply barriers");
 // TMEM columns: S fp32 0..127 (M = 128), P 128..191 (M = 64), O[0] 192..327, O[1] 352..487 (M = 64)
 constexpr uint32_t kTS32 = 0, kTP = 128, kTO0 = 192, kTO1 = 352;
 constexpr int kGN = 136;
 constexpr uint32_t kGIdP = tc::idesc_bf16(64, 64, false, false);    // A = q, B = k (both K-major)
 constexpr uint32_t kGIdS = tc::idesc_bf16(128, 128, true, true);    // A = v^T, B = k (both MN-major)
 constexpr uint32_t kGIdQ = tc::idesc_bf16(64, kGN, false, false);   // A = q, B = [h_c^T ; z_c] (both K-major)
-constexpr uint32_t kGIdV = tc::idesc_bf16(64, kGN, false, true);    // A = P (K-major), B = [v | 1] (MN-major)
+constexpr uint32_t kGIdV = tc::idesc_bf16(64, 128, false, true);   // A = P (K-major), B = v (MN-major)
+constexpr uint32_t kGIdV1 = tc::idesc_bf16(64, kGN, false, true);   // A = P, B = [v | ones] (MN-major, three boxes)
+constexpr uint32_t kGId1 = tc::idesc_bf16(64, 8, false, true);      // A = P (K-major), B = the ones tile (MN-major)
 
 // Cross-CTA counters of the fused form (gpu scope).
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
@@ -652,6 +672,10 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    float* __restrict__ zs, int normalize, __nv_bfloat16* __restrict__ o, int* __restrict__ counters,
                    float* __restrict__ Sg, float* __restrict__ zg, const float* __restrict__ h0,
                    float* __restrict__ h_T, float* __restrict__ z_T) {
+    using GL = GLayout<FUSED>;
+    constexpr int kGStages = GL::kStages;
+    constexpr uint32_t kGStage = GL::kStage, kGSnap = GL::kSnap, kGP = GL::kP, kGOnes = GL::kOnes, kGO = GL::kO,
+                       kGBarOff = GL::kBarOff;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -688,11 +712,11 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int n1 = FUSED ? nc : 0;  // phase-1 loads before the apply's
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     auto bar = [&](int i) { return sbase + kGBarOff + 8u * (uint32_t)i; };
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + kGBarOff + 112);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sptr + kGBarOff + kGFlag);
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quadrant
 
     if (tid == 0) {
-        for (int b = 0; b < G_COUNT; ++b) tc::mbar_init(bar(b), (b == G_EMPTY || b == G_EMPTY + 1) ? 2 : 1);
+        for (int b = 0; b < G_COUNT; ++b) tc::mbar_init(bar(b), (b >= G_EMPTY && b < G_EMPTY + kGStages) ? 2 : 1);
         tc::fence_mbar_init();
         abort_flag[0] = 0;
         abort_flag[1] = hdr->wait_limit;
@@ -702,11 +726,11 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tc::prefetch_tmap(&tm_o);
     }
     __syncwarp();
-    if (warp == 0) tc::tmem_alloc(sbase + kGBarOff + 120, 512);
+    if (warp == 0) tc::tmem_alloc(sbase + kGBarOff + kGSlot, 512);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t*>(sptr + kGBarOff + 120), 0);
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t*>(sptr + kGBarOff + kGSlot), 0);
 
     if (warp == 0) {
         // ---- TMA: load l (phase-1 k, v for l < n1, then q, k, v of chunk l - n1) into stage l % kGStages
@@ -752,13 +776,12 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc::commit_e(bar(G_EMPTY + s));
         }
         if (FUSED) tc::commit_e(bar(G_SD));  // phase 1 done: the state group may read S (phase 0 of G_SD)
-        const int sd0 = FUSED ? 1 : 0;        // G_SD phases taken before the apply's
         // the apply, chunk by chunk
         for (int i = 0; i < nc; ++i) {
             const int l = n1 + i, s = l % kGStages, b = i & 1;
             const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
             const uint32_t st = sbase + s * kGStage, q0 = st, k0 = st + 16384, v0 = st + 32768;
-            const uint32_t snap = sbase + kGSnap + 2 * kGSnapBox * (uint32_t)b;
+            const uint32_t snap = sbase + kGSnap + (GL::kCopies == 2 ? 2 * kGSnapBox * (uint32_t)b : 0u);
             const uint32_t dO = tmem + (b ? kTO1 : kTO0);
             if (!warp_wait(bar(G_FULL + s), (l / kGStages) & 1, ws, abort_flag, 4301)) break;
             if (r.n < kChunk) {  // the state group first zeroes the rows past the sequence's end
@@ -775,21 +798,27 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!warp_wait(bar(G_SNAP), i & 1, ws, abort_flag, 4303)) break;
             tc::tc_fence_after();
             tc::mma_ss_n<4>(tmem + kTS32, tc::sdesc(v0, 8192, 1024), 128, tc::sdesc(k0, 8192, 1024), 128, kGIdS, true);
-            tc::commit_e(bar(G_SD));
+            if (GL::kCopies == 2) tc::commit_e(bar(G_SD));  // S updated; the other copy was read by chunk i - 1
             // O[b] = q [h_c | z_c] once chunk i - 2's O[b] has been read
             if (i >= 2 && !warp_wait(bar(G_OFREE + b), ((i >> 1) - 1) & 1, ws, abort_flag, 4304)) break;
             tc::tc_fence_after();
             tc::mma_ss_n<4>(dO, tc::sdesc(q0, 16, 1024), 2, tc::sdesc(snap, 16, 1024), 2, kGIdQ, false);
             tc::mma_ss_n<4>(dO, tc::sdesc(q0 + 8192, 16, 1024), 2, tc::sdesc(snap + kGSnapBox, 16, 1024), 2, kGIdQ,
                             true);
-            // O[b] += P [v | 1] once P is masked and stored
+            if (GL::kCopies == 1) tc::commit_e(bar(G_SD));  // S updated and the one copy read
+            // O[b] += P v, O[b][128..135] += P 1 once P is masked and stored
             if (!warp_wait(bar(G_PREADY), i & 1, ws, abort_flag, 4305)) break;
             tc::tc_fence_after();
-            tc::mma_ss_n<4>(dO, tc::sdesc(sbase + kGP, 16, 1024), 2, tc::sdesc(v0, 8192, 1024), 128, kGIdV, true);
+            if (GL::kOnesInStage) {
+                tc::mma_ss_n<4>(dO, tc::sdesc(sbase + kGP, 16, 1024), 2, tc::sdesc(v0, 8192, 1024), 128, kGIdV1, true);
+            } else {
+                tc::mma_ss_n<4>(dO, tc::sdesc(sbase + kGP, 16, 1024), 2, tc::sdesc(v0, 8192, 1024), 128, kGIdV, true);
+                tc::mma_ss_n<4>(dO + 128, tc::sdesc(sbase + kGP, 16, 1024), 2, tc::sdesc(sbase + kGOnes, 8192, 1024),
+                                128, kGId1, true);
+            }
             tc::commit_e(bar(G_OD + b));
             tc::commit_e(bar(G_EMPTY + s));
         }
-        (void)sd0;
         tc::commit_e(bar(G_FIN));
         __syncwarp();
     } else if (warp < 6) {
@@ -825,14 +854,15 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc::named_bar(1, 128);
             if (leader) tc::mbar_arrive(bar(G_ZREADY));
         };
-        // fixed parts: the ones column after v in both stages (row s, column 0 of the
-        // third box), rows 128..135 of both snapshots zero
-        for (int x = f; x < kGStages * 64 * 8; x += 128) {
-            const int stg = x >> 9, row = (x >> 3) & 63, c = x & 7;
-            tc::st_shared_v4(sbase + (uint32_t)stg * kGStage + 49152 + (uint32_t)row * 128 + (uint32_t)c * 16,
-                             c == (row & 7) ? 0x3F80u : 0u, 0u, 0u, 0u);
+        // fixed parts: the ones (row s: 1 in column 0, the first element of its logical
+        // 16-byte chunk 0) in the ones tile or after v in every stage, rows 128..135 of
+        // the state copies zero
+        for (int x = f; x < (GL::kOnesInStage ? kGStages : 1) * 64 * 8; x += 128) {
+            const int box = x >> 9, row = (x >> 3) & 63, c = x & 7;
+            const uint32_t base = GL::kOnesInStage ? sbase + (uint32_t)box * kGStage + 49152 : sbase + kGOnes;
+            tc::st_shared_v4(base + (uint32_t)row * 128 + (uint32_t)c * 16, c == (row & 7) ? 0x3F80u : 0u, 0u, 0u, 0u);
         }
-        for (int x = f; x < 4 * 8 * 8; x += 128) {
+        for (int x = f; x < GL::kCopies * 2 * 8 * 8; x += 128) {
             const int box = x >> 6, row = 128 + ((x >> 3) & 7), c = x & 7;
             tc::st_shared_v4(sbase + kGSnap + (uint32_t)box * kGSnapBox + (uint32_t)row * 128 + (uint32_t)c * 16, 0u,
                              0u, 0u, 0u);
@@ -881,18 +911,45 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const int per = ((kD * kD / ng) + 3) & ~3;
                 const int e0 = min(kD * kD, jg * per), e1 = min(kD * kD, e0 + per);
                 const size_t ub = (size_t)u * kD * kD;
-                for (int e = e0 + 4 * f; e < e1; e += 4 * 128) {
-                    float4 acc = h0 ? *reinterpret_cast<const float4*>(h0 + ub + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int gg = 0; gg < ng; ++gg) {  // (L2 loads: other CTAs of this launch wrote Sg)
-                        const size_t at = ((gb + gg) * H + head) * kD * kD + e;
-                        const float4 d = __ldcg(reinterpret_cast<const float4*>(Sg + at));
-                        *reinterpret_cast<float4*>(hs + at) = acc;
-                        acc.x += d.x;
-                        acc.y += d.y;
-                        acc.z += d.z;
-                        acc.w += d.w;
+                // two float4 positions per thread and four groups at a time, all eight loads
+                // issued before the running sums take them (L2 loads: other CTAs of this
+                // launch wrote Sg)
+                const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                auto add4 = [](float4& a, const float4& d) {
+                    a.x += d.x;
+                    a.y += d.y;
+                    a.z += d.z;
+                    a.w += d.w;
+                };
+                for (int e = e0 + 4 * f; e < e1; e += 2 * 4 * 128) {
+                    const bool two = e + 4 * 128 < e1;
+                    float4 a0 = h0 ? *reinterpret_cast<const float4*>(h0 + ub + e) : zero4;
+                    float4 a1 = (h0 && two) ? *reinterpret_cast<const float4*>(h0 + ub + e + 512) : zero4;
+                    for (int gg = 0; gg < ng; gg += 4) {
+                        float4 d0[4], d1[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const bool on = gg + u < ng;
+                            const size_t at = ((gb + gg + u) * H + head) * kD * kD + e;
+                            d0[u] = on ? __ldcg(reinterpret_cast<const float4*>(Sg + at)) : zero4;
+                            d1[u] = (on && two) ? __ldcg(reinterpret_cast<const float4*>(Sg + at + 512)) : zero4;
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (gg + u >= ng) break;
+                            const size_t at = ((gb + gg + u) * H + head) * kD * kD + e;
+                            *reinterpret_cast<float4*>(hs + at) = a0;
+                            add4(a0, d0[u]);
+                            if (two) {
+                                *reinterpret_cast<float4*>(hs + at + 512) = a1;
+                                add4(a1, d1[u]);
+                            }
+                        }
                     }
-                    if (h_T) *reinterpret_cast<float4*>(h_T + ub + e) = acc;
+                    if (h_T) {
+                        *reinterpret_cast<float4*>(h_T + ub + e) = a0;
+                        if (two) *reinterpret_cast<float4*>(h_T + ub + e + 512) = a1;
+                    }
                 }
                 if (jg == 0) {
                     float zacc = 0.f;
@@ -950,7 +1007,7 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     // the state after this chunk, for the next one
                     if (!group_wait(leader, 1, bar(G_SD), (sd0 + i) & 1, ws, abort_flag, 4307)) break;
                     tc::tc_fence_after();
-                    const uint32_t snap = sbase + kGSnap + 2 * kGSnapBox * (uint32_t)((i + 1) & 1);
+                    const uint32_t snap = sbase + kGSnap + (GL::kCopies == 2 ? 2 * kGSnapBox * (uint32_t)((i + 1) & 1) : 0u);
 #pragma unroll 1
                     for (int half = 0; half < 2; ++half) {
                         float x[64], y[32];
@@ -1016,8 +1073,12 @@ group_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int i = 0; i < nc; ++i) {
             const int b = i & 1;
             const ChunkRef r = chunk_ref(cu, chunk_off, n_seqs, c0 + i);
-            const uint32_t tO = tmem + lane_off + (b ? kTO1 : kTO0), stage_o = sbase + kGO + 16384u * (uint32_t)b;
-            if (leader) tc::bulk_wait_read1();  // the store from this staging tile two chunks back is done reading it
+            const uint32_t tO = tmem + lane_off + (b ? kTO1 : kTO0);
+            const uint32_t stage_o = sbase + kGO + (GL::kOTiles == 2 ? 16384u * (uint32_t)b : 0u);
+            if (leader) {  // the store that last read this staging tile is done reading it
+                if (GL::kOTiles == 2) tc::bulk_wait_read1();
+                else tc::bulk_wait_read0();
+            }
             if (!group_wait(leader, 3, bar(G_OD + b), (i >> 1) & 1, ws, abort_flag, 4309)) break;
             tc::tc_fence_after();
             float inv = 1.f;
@@ -1190,7 +1251,8 @@ cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* ext
         __nv_bfloat16* o = (__nv_bfloat16*)a.o;
         const int nrm = normalize ? 1 : 0;
         if (fused) {
-            e = cudaFuncSetAttribute(group_apply_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+            e = cudaFuncSetAttribute(group_apply_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)GLayout<true>::kSmem);
             if (e != cudaSuccess) return e;
             int H = a.H;
             char* ws = plan_ws;
@@ -1198,7 +1260,7 @@ cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* ext
             void* args[] = {&mq, &mk, &mv, &mo, &H, &ws, &group_off, &hs, &zs, (void*)&nrm, &o, &counters, &Sg, &zg,
                             (void*)&h0, &h_T, &z_T};
             return cudaLaunchCooperativeKernel((const void*)group_apply_kernel<true>, dim3((unsigned)sms),
-                                               dim3(kGThreads), args, kGSmem, st);
+                                               dim3(kGThreads), args, GLayout<true>::kSmem, st);
         }
         e = cudaFuncSetAttribute(kv_reduce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmem);
         if (e != cudaSuccess) return e;
@@ -1208,9 +1270,10 @@ cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* ext
         group_scan_kernel<<<dim3((unsigned)a.n_seqs, a.H, kD / kScanCols), kD, 0, st>>>(plan_ws, group_off, a.H, a.h0,
                                                                                        Sg, zg, hs, zs, h_T, z_T);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(group_apply_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+        e = cudaFuncSetAttribute(group_apply_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)GLayout<false>::kSmem);
         if (e != cudaSuccess) return e;
-        group_apply_kernel<false><<<dim3((unsigned)ng, a.H), kGThreads, kGSmem, st>>>(
+        group_apply_kernel<false><<<dim3((unsigned)ng, a.H), kGThreads, GLayout<false>::kSmem, st>>>(
             mq, mk, mv, mo, a.H, plan_ws, group_off, hs, zs, nrm, o, nullptr, nullptr, nullptr, nullptr, nullptr,
             nullptr);
         return cudaGetLastError();
