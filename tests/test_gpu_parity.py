@@ -463,6 +463,30 @@ def test_linear_bidirectional_forced_timeout_then_recovery(g):
     assert rel(o, ro) <= TOL["bf16"]
 
 
+# ------------------------------------------------------------------ the plan at the one-warp boundary
+
+@pytest.mark.parametrize("n_seqs", [32, 33])
+def test_plan_boundary_gdn_and_linear(g, monkeypatch, n_seqs):
+    """32 sequences take the plan's one-warp path (one lane copies two offsets),
+    33 the block-wide one: every output and final state of GDN and of the
+    grouped linear attention against the oracle (ragged lengths, an empty
+    sequence, a one-token one)."""
+    monkeypatch.delenv("GDN_LINEAR_PATH", raising=False)
+    gen = torch.Generator().manual_seed(70 + n_seqs)
+    lengths = [int(x) for x in torch.randint(1, 300, (n_seqs,), generator=gen)]
+    lengths[3], lengths[7] = 0, 1
+    inp = gi.gdn_inputs(lengths, 2, 128, 128, "bf16", h0_std=0.01, seed=71)
+    o, hT = run_gdn(g, inp)
+    ro, rh = ref_gdn(inp)
+    assert rel(o, ro) <= TOL["bf16"] and rel(hT, rh) <= TOL["bf16"]
+    lin = gi.linear_inputs(lengths, 2, 128, 128, "bf16", h0_std=0.1, seed=72)
+    d = dev(lin)
+    o2, h2, ws = g.linear_attn_fwd(d["q"], d["k"], d["v"], d["h0"], d["cu_seqlens"])
+    assert g.workspace_status(ws) == 0
+    ro2, rh2 = oracle.linear(lin["q"], lin["k"], lin["v"], lin["h0"], lin["cu_seqlens"])
+    assert rel(o2, ro2) <= TOL["bf16"] and rel(h2, rh2) <= TOL["bf16"]
+
+
 # ------------------------------------------------------------------ causal linear attention, grouped
 
 @pytest.mark.parametrize("fused", [True, False])
