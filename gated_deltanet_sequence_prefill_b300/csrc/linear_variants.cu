@@ -497,10 +497,12 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 // ---------------------------------------------------------------- causal, grouped
 // Causal linear attention without a per-chunk chain across the whole
-// sequence: every sequence is cut into groups of `group` chunks; the groups'
-// K^T V (kv_reduce_kernel<true>) give each group's starting state by a prefix
-// (group_scan_kernel), and every group then runs its own chunks in order from
-// that state (group_apply_kernel), all groups side by side.
+// sequence: every sequence is cut into groups of chunks (the size is picked by
+// the call's plan kernel); the groups' K^T V (kv_reduce_kernel<true>) give
+// each group's starting state by a prefix (group_scan_kernel), and every group
+// then runs its own chunks in order from that state (group_apply_kernel<false>),
+// all groups side by side.  Small problems do all three in one cooperative
+// launch (group_apply_kernel<true>).
 
 // Per (sequence, head, 8 state columns): each group's starting state
 // hs[g] = h0 + the K^T V of the sequence's earlier groups (fp32; group g's
