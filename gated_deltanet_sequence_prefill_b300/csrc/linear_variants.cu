@@ -1261,8 +1261,12 @@ cudaError_t launch_linear_grouped(const PrefillArgs& a, char* plan_ws, char* ext
             const float* h0 = a.h0;
             void* args[] = {&mq, &mk, &mv, &mo, &H, &ws, &group_off, &hs, &zs, (void*)&nrm, &o, &counters, &Sg, &zg,
                             (void*)&h0, &h_T, &z_T};
-            return cudaLaunchCooperativeKernel((const void*)group_apply_kernel<true>, dim3((unsigned)sms),
-                                               dim3(kGThreads), args, GLayout<true>::kSmem, st);
+            e = cudaLaunchCooperativeKernel((const void*)group_apply_kernel<true>, dim3((unsigned)sms),
+                                            dim3(kGThreads), args, GLayout<true>::kSmem, st);
+            if (e != cudaErrorCooperativeLaunchTooLarge && e != cudaErrorNotSupported) return e;
+            // cooperative launches refused here (e.g. a shared device): the same groups
+            // through the separate kernels below
+            (void)cudaGetLastError();
         }
         e = cudaFuncSetAttribute(kv_reduce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmem);
         if (e != cudaSuccess) return e;
