@@ -317,18 +317,19 @@ kv_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 
 // ---------------------------------------------------------------- apply
 // B operand [K^T V | z] (rows i, three 64-column SW128 boxes: columns
-// 0..63, 64..127, and z in column 128 with zeros after it), a ring of q
-// tiles, two o staging tiles, the barriers.  D = q [K^T V | z] (M = 64,
-// N = 136) in one of two TMEM buffers: columns 0..127 the numerator, 128
-// the normaliser q . z.
-constexpr int kAStages = 3;
-constexpr uint32_t kAKVZ = 0, kAQ = 49152, kAO = kAQ + kAStages * 16384, kABarOff = kAO + 2 * 16384;
+// 0..63, 64..127, and z in column 128 with zeros after it), a two-stage ring
+// of q tiles, one o staging tile, the barriers: ~97 KB, and 256 TMEM columns
+// with D = q [K^T V | z] (M = 64, N = 136: columns 0..127 the numerator, 128
+// the normaliser q . z) single-buffered, so that two CTAs share an SM and
+// one's epilogue overlaps the other's loads and MMAs.
+constexpr int kAStages = 2;
+constexpr uint32_t kAKVZ = 0, kAQ = 49152, kAO = kAQ + kAStages * 16384, kABarOff = kAO + 16384;
 enum { A_FULL = 0, A_EMPTY = 3, A_MMAD = 6, A_EPID = 8, A_KVR = 10, A_FIN = 11, A_COUNT = 12 };
 constexpr uint32_t kASmem = kABarOff + 128 + 1024;
 constexpr int kAN = 136;
 constexpr uint32_t kIdQ = tc::idesc_bf16(64, kAN, false, true);  // A = q (K-major), B = [K^T V | z] (MN-major)
 
-__global__ void __launch_bounds__(kLvThreads, 1)
+__global__ void __launch_bounds__(kLvThreads, 2)
 kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o, int H,
                 int group, char* __restrict__ ws, const float* __restrict__ kv, const float* __restrict__ z,
                 int normalize, __nv_bfloat16* __restrict__ o) {
@@ -359,7 +360,7 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc::prefetch_tmap(&tm_o);
     }
     __syncwarp();
-    if (warp == 0) tc::tmem_alloc(sbase + kABarOff + 104, 512);
+    if (warp == 0) tc::tmem_alloc(sbase + kABarOff + 104, 256);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -396,9 +397,9 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ++runs;
             }
             if (!warp_wait(bar(A_FULL + s), (i / kAStages) & 1, ws, abort_flag, 4202)) break;
-            if (i >= 2 && !warp_wait(bar(A_EPID + b), ((i >> 1) - 1) & 1, ws, abort_flag, 4203)) break;
+            if (i >= 1 && !warp_wait(bar(A_EPID + ((i - 1) & 1)), ((i - 1) >> 1) & 1, ws, abort_flag, 4203)) break;
             tc::tc_fence_after();
-            const uint32_t st = sbase + kAQ + s * 16384, d = tmem + 256u * b;
+            const uint32_t st = sbase + kAQ + s * 16384, d = tmem;
             tc::mma_ss_n<4>(d, tc::sdesc(st, 16, 1024), 2, tc::sdesc(sbase + kAKVZ, 16384, 1024), 128, kIdQ, false);
             tc::mma_ss_n<4>(d, tc::sdesc(st + 8192, 16, 1024), 2, tc::sdesc(sbase + kAKVZ + 64 * 128, 16384, 1024), 128,
                             kIdQ, true);
@@ -446,44 +447,51 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             if (!group_wait(leader, 1, bar(A_MMAD + b), (i >> 1) & 1, ws, abort_flag, 4204)) break;
             tc::tc_fence_after();
-            float d[32], e[16];
-            uint32_t pk[64];
-            tc::tmem_ld16(tmem + 256u * b + ((uint32_t)(32 * (warp & 3)) << 16) + 128, e);
+            const bool full = r.n == kChunk;
+            const uint32_t ob = sbase + kAO;
+            if (full) {  // the previous store is done reading the staging tile
+                if (leader) tc::bulk_wait_read0();
+                tc::named_bar(1, 128);
+            }
+            float e[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128, e);
             tc::tmem_wait_ld();
             const float inv = normalize ? 1.f / e[0] : 1.f;
-#pragma unroll
+            // o in four parts of 32 columns, each staged (or stored) as soon as it is packed
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
-                tc::tmem_ld32(tmem + 256u * b + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * c, d);
+                float d[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * c, d);
                 tc::tmem_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) pk[16 * c + x] = tc::pack_bf16(d[2 * x] * inv, d[2 * x + 1] * inv);
+                for (int x = 0; x < 16; ++x) pk[x] = tc::pack_bf16(d[2 * x] * inv, d[2 * x + 1] * inv);
+                if (full) {
+                    if (lane < 16) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int c16 = 4 * c + q4;
+                            tc::st_shared_v4(tc::sw128(ob + (uint32_t)(c16 >> 3) * 8192, t, c16 & 7), pk[4 * q4],
+                                             pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                        }
+                    }
+                } else if (lane < 16 && t < r.n) {  // the last, partial chunk of a sequence
+                    uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(r.t0 + t) * H + head) * kD) + 4 * c;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                }
             }
+            tc::fence_proxy_async();
             tc::tc_fence_before();
             tc::named_bar(1, 128);
-            if (leader) tc::mbar_arrive(bar(A_EPID + b));  // D[b] may be overwritten
-            if (r.n == kChunk) {
-                // stage o in SW128 boxes and store it with the tensor map
-                const uint32_t ob = sbase + kAO + (uint32_t)b * 16384;
-                if (leader) tc::bulk_wait_read0();  // earlier stores are done reading the staging tiles
-                tc::named_bar(1, 128);
-                if (lane < 16) {
-#pragma unroll
-                    for (int c16 = 0; c16 < 16; ++c16)
-                        tc::st_shared_v4(tc::sw128(ob + (uint32_t)(c16 >> 3) * 8192, t, c16 & 7), pk[4 * c16],
-                                         pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-                }
-                tc::fence_proxy_async();
-                tc::named_bar(1, 128);
-                if (leader) {
+            if (leader) {
+                tc::mbar_arrive(bar(A_EPID + b));  // D may be overwritten
+                if (full) {
                     tc::tma_store_3d(&tm_o, ob, 0, head, r.t0);
                     tc::tma_store_3d(&tm_o, ob + 8192, 64, head, r.t0);
                     tc::bulk_commit();
                 }
-            } else if (lane < 16 && t < r.n) {  // the last, partial chunk of a sequence
-                uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(r.t0 + t) * H + head) * kD);
-#pragma unroll
-                for (int c16 = 0; c16 < 16; ++c16)
-                    dst[c16] = make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
             }
         }
         if (leader) tc::bulk_wait0();
@@ -492,7 +500,7 @@ kv_apply_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (tid == 0) tc::mbar_wait(bar(A_FIN), 0);
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(tmem, 512);
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------- causal, grouped
