@@ -141,7 +141,7 @@ __device__ __forceinline__ void group_range(const int* group_off, const int* chu
 //   group_off[n_seqs + 1]) and writes its K^T V and key sums to
 //   kv[2 g + p][head], z[2 g + p][head].
 template <bool GROUPED>
-__global__ void __launch_bounds__(kLvThreads, 1)
+__global__ void __launch_bounds__(kLvThreads, 2)  // two CTAs per SM (registers <= 128)
 kv_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, int H,
                  int group, char* __restrict__ ws, const int* __restrict__ group_off, float* __restrict__ kv,
                  float* __restrict__ z) {
